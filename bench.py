@@ -1,0 +1,384 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused post-backward ZeRO step (ring reduce-scatter + unscale + overflow check +
+AdamW + cast + all-gather write) on GB300.
+
+Default workload: the 1.3B transformer shapes (145 tensors, 1,311,080,448 params, 33 buckets of at
+most 50M params), W = 8 emulated workers, bf16 gradients and parameters, ZeRO-3 memory plan. One step
+is one launch of the fused kernel over every bucket. Inputs (55 GB read+written per step) are far
+larger than the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line: Gparams/s (value), the roofline of the fused kernel against the measured HBM
+copy bandwidth, the oracle timed on the host cores (cpu_baseline), and the end-to-end rate through
+zr_step_from_host with pinned host gradients (e2e).
+
+--impl reference times the CPU oracle (the only reference this method has) on the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD_DEFAULT = "1p3b"
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _traffic_record(workload: str):
+    """Per-launch DRAM bytes of the fused kernel from the committed ncu summary, if the kernel source has
+    not changed since it was taken (the summary records the source hash)."""
+    import hashlib
+    src = os.path.join(ROOT, "zero_gradient_reduction_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("zr_step.cu", "zr_device.cuh"):
+        with open(os.path.join(src, f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", f"fused_step_{workload}.md")
+    if not os.path.exists(path):
+        return None, digest
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                rec[k.strip()] = v.strip().strip("`")
+    if rec.get("kernel_source_sha256_16") != digest:
+        return None, digest
+    try:
+        return float(rec["traffic_bytes_per_launch"]), digest
+    except Exception:
+        return None, digest
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return out
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return out
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        load = [s for s, p in zip(sm, power) if p > 300.0] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        out.update(sm_mhz=statistics.median(load) if load else None, sm_max_mhz=max(mx) if mx else None,
+                   reasons=reasons, samples=len(rows), power_w_max=max(power) if power else None)
+        return out
+
+
+def oracle_sample(w, plan_buckets, offsets, seconds_target: float, max_buckets: int = 64, window: int = 0):
+    """Time the CPU oracle on whole buckets (window == 0) or on a mini-bucket of `window` elements per ring
+    block taken from bucket 0, until about `seconds_target` of oracle time is spent. Returns
+    (params processed, oracle seconds, description)."""
+    import oracle
+    import zrgen
+    from zrgen.layout import Layout
+    sig = zrgen.sigma_per_tensor(w)
+    layout = Layout(w.tensors, offsets, sig, w.seed, w.dtype, w.master_sigma)
+    total_params, total_s, used = 0, 0.0, 0
+    hyper = oracle.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    for b in range(min(len(plan_buckets), max_buckets)):
+        start, n, C = (int(x) for x in plan_buckets[b])
+        if window:
+            idx = np.concatenate([np.arange(start + c * C, start + c * C + min(window, max(0, n - c * C)))
+                                  for c in range(w.W)])
+            Cw = window
+        else:
+            idx = np.arange(start, start + n)
+            Cw = C
+        lo = idx
+        grads = []
+        runs = np.flatnonzero(np.diff(lo) != 1) + 1
+        for r in range(w.W * w.A):
+            g = np.empty(len(lo), np.uint16)
+            for seg in np.split(np.arange(len(lo)), runs):
+                a, e = int(lo[seg[0]]), int(lo[seg[-1]]) + 1
+                g[seg] = layout.grads_host(a, e, 1, r, w.init_scale)
+            grads.append(g)
+        master = np.empty(len(lo), np.float32)
+        for seg in np.split(np.arange(len(lo)), runs):
+            a, e = int(lo[seg[0]]), int(lo[seg[-1]]) + 1
+            master[seg] = layout.master_host(a, e)
+        m = np.zeros(len(lo), np.float32)
+        v = np.zeros(len(lo), np.float32)
+        p = np.zeros(len(lo), np.uint16)
+        sc = oracle.new_scaler(w.init_scale, w.dynamic)
+        t0 = time.perf_counter()
+        oracle.step(w.W, w.A, w.dtype, np.array([[0, len(lo), Cw]]), grads, master, m, v, p, hyper, sc)
+        total_s += time.perf_counter() - t0
+        total_params += len(lo)
+        used += 1
+        if total_s >= seconds_target:
+            break
+    what = (f"{used} whole bucket(s) of the {w.name} workload ({total_params} params, W={w.W})" if not window else
+            f"{used} mini-bucket(s) of {window} params per ring block of the {w.name} workload "
+            f"({total_params} params, W={w.W})")
+    return total_params, total_s, what
+
+
+def run_reference(args, w):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    import zrgen
+    oracle.build()
+    zrgen.build_host()
+    b, offs = oracle.bucket_plan(list(w.tensors), w.cap, w.W)
+    # every step: one mini-bucket of 32768 params per ring block, timed on one host core
+    for _ in range(args.warmup):
+        oracle_sample(w, b, offs, 0.0, max_buckets=1, window=32768)
+    params, secs = 0, 0.0
+    what = ""
+    for _ in range(args.steps):
+        p, s, what = oracle_sample(w, b, offs, 0.0, max_buckets=1, window=32768)
+        params += p
+        secs += s
+    value = params / secs / 1e9
+    ms = secs / args.steps * 1e3
+    line = {
+        "impl": "reference", "metric": "fused reduce-scatter+AdamW step Gparams/s", "value": value,
+        "unit": "Gparams/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": _config(w, b, "oracle on host cores; per step a sample of the workload"),
+        "cpu_baseline": {"value": value, "unit": "Gparams/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step: {what}"},
+        "e2e": {"value": value, "unit": "Gparams/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w, buckets, l2_note):
+    return {"workload": f"{w.name}: {w.description}", "W": w.W, "A": w.A, "stage": w.stage,
+            "params": w.n, "buckets": int(len(buckets)), "grad_dtype": "fp16" if w.dtype == 0 else "bf16",
+            "state_dtype": "fp32 master/m/v (ping-pong sets)",
+            "alg_bytes_per_param": w.alg_bytes_per_param(), "l2": l2_note, "parallelism": "replicas"}
+
+
+def run_zr(args, w):
+    import torch
+    ws, rank, local = _dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device(f"cuda:{local if ws > 1 else 0}")
+
+    import __graft_entry__
+    if rank == 0 or ws == 1:
+        __graft_entry__.build()
+    if ws > 1:
+        torch.distributed.barrier()
+        __graft_entry__.build()  # no-op once built
+    import zero_gradient_reduction_gb300 as zr
+    import zrgen
+    from zrgen.layout import Layout
+
+    plan = zr.Plan(list(w.tensors), W=w.W, A=w.A, dtype=w.dtype, stage=w.stage, cap=w.cap,
+                   scaler=zr.Scaler(w.init_scale, w.dynamic))
+    hyper = zr.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    layout = Layout(w.tensors, plan.tensor_offsets, zrgen.sigma_per_tensor(w), w.seed, w.dtype, w.master_sigma)
+    stream = torch.cuda.current_stream(dev)
+    cs = stream.cuda_stream
+    table = torch.from_numpy(zrgen.normal_table().copy()).to(dev)
+    n = plan.numel
+    state = plan.new_state(dev)
+    state.master[0].zero_()
+    layout.master_dev(state.master[0], table, cs)
+    zr.all_gather(state.master[0], [state.param[0]])
+    grads = [torch.zeros(n, dtype=plan.torch_dtype(), device=dev) for _ in range(w.W * w.A)]
+    for r in range(w.W * w.A):
+        layout.grads_dev(grads[r], 1, r, w.init_scale, table, cs)
+    torch.cuda.synchronize(dev)
+
+    def timed(k):
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            plan.step(grads, state, hyper, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if ws > 1:
+            torch.distributed.barrier()
+        return e0.elapsed_time(e1)
+
+    for _ in range(args.warmup):
+        plan.step(grads, state, hyper, stream=stream)
+    torch.cuda.synchronize(dev)
+
+    attempts = 0
+    while True:
+        sampler = ClockSampler(local if ws > 1 else 0)
+        sampler.start()
+        ms_total = timed(args.steps)
+        clocks = sampler.stop()
+        attempts += 1
+        bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"} & set(clocks.get("reasons", []))
+        if not bad or attempts >= 2:
+            break
+    rep = plan.report(stream)
+    assert rep.overflow == 0 and rep.steps == args.warmup + args.steps * attempts, rep.as_dict()
+
+    ms_max = ms_total
+    if ws > 1:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    value = ws * plan.n_real / (ms_step * 1e-3) / 1e9
+
+    # roofline of the fused kernel: one launch per step, algorithmic bytes (2*W*A + 26) per param
+    peak, peak_kind = _peaks()
+    achieved = rep.bytes_alg / (ms_total / args.steps * 1e-3) / 1e9
+    traffic, _digest = _traffic_record(w.name)
+
+    e2e = None
+    cpu = None
+    if not args.no_e2e:
+        # end to end through the public API: pinned host gradients copied in every step, report read back
+        host = [torch.empty(n, dtype=plan.torch_dtype(), pin_memory=True) for _ in range(w.W * w.A)]
+        for r in range(w.W * w.A):
+            host[r].copy_(grads[r])
+        dgr = [torch.empty_like(g) for g in grads]
+        plan.step_from_host(host, dgr, state, hyper, stream=stream)  # warm
+        if ws > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            r = plan.step_from_host(host, dgr, state, hyper, stream=stream)
+        dt = time.perf_counter() - t0
+        if ws > 1:
+            t = torch.tensor([dt], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": ws * plan.n_real * args.e2e_steps / dt / 1e9, "unit": "Gparams/s",
+               "h2d_bytes_per_step": int(2 * n * w.W * w.A), "d2h_bytes_per_step": int(__import__("ctypes").sizeof(r)),
+               "ms_per_step": dt / args.e2e_steps * 1e3, "steps": args.e2e_steps,
+               "api": "zr_step_from_host (pinned host grads -> device, fused step, report read back)"}
+        del host, dgr
+
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        params, secs, what = oracle_sample(w, plan.buckets, plan.tensor_offsets, args.cpu_seconds)
+        cpu = {"value": params / secs / 1e9, "unit": "Gparams/s", "cores": 1, "kind": "oracle",
+               "sample": f"{what}, step 1 inputs; {secs:.1f} s single-threaded on the host"}
+
+    line = {
+        "metric": "fused reduce-scatter+AdamW step Gparams/s", "value": value, "unit": "Gparams/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded Philox4x32-10 normal draws, the workload's shapes and sigmas)",
+        "config": _config(w, plan.buckets, f"inputs larger than L2: {rep.bytes_alg / 1e9:.1f} GB moved per step"),
+        "hbm_tbs": achieved / 1e3,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "frac_of_8tbs_nominal": achieved / 8000.0,
+                     "kernel": "fused_step_kernel (one launch per step)"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
+                   "reasons": clocks.get("reasons"), "samples": clocks.get("samples"),
+                   "power_w_max": clocks.get("power_w_max"), "attempts": attempts},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["zr", "reference"], default="zr")
+    ap.add_argument("--workload", default=WORKLOAD_DEFAULT)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print(f"bench: raising --warmup {args.warmup} to the minimum of 3", file=sys.stderr)
+        args.warmup = 3
+    import zrgen
+    w = zrgen.workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_zr(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

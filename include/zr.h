@@ -1,0 +1,256 @@
+/*
+ * zr.h — C ABI of libzr: the data-parallel step that runs after backward, on one GB300.
+ *
+ * W data-parallel workers are emulated as W gradient replicas resident in one GPU's
+ * HBM. The step ring-reduce-scatters their gradient buckets, removes the loss scale
+ * and takes the mean, checks for overflow, runs a mixed-precision AdamW update of
+ * each owner's fp32 master/m/v shard, casts the shard to fp16/bf16 and all-gathers
+ * it into the full parameter replica.
+ *
+ * Pages the operations follow (cited by title and section):
+ *  [P1] "DP / DDP / DeepSpeed ZeRO-1/2/3" (gitcode.csdn.net): 二 DDP — ring
+ *       all-reduce walk-through (scatter reduce, then all-gather), reverse-order
+ *       buckets, per-GPU traffic; 三 ZeRO-1 — owners average, convert to FP32,
+ *       scale, update m, v, master, then the FP16 params, and broadcast them;
+ *       四 ZeRO-2/3 — gradient and parameter sharding.
+ *  [P2] "并行训练框架DeepSpeed介绍" (nanhubrain.csdn.net): 核心技术 (1)-(3) mixed
+ *       precision, BF16/FP16, dynamic loss scaling; (11)-(13) ZeRO-1/2/3 flows.
+ *  [P3] "第 7 讲：Parallelism（上）" (CS336 lecture 7): memory table (16 bytes per
+ *       parameter), Ring AllReduce = ReduceScatter + AllGather, ZeRO stage memory
+ *       formulas, gradient accumulation, torch.optim.AdamW in the DDP loop.
+ *
+ * Conventions for every call:
+ *  - Device pointers point into memory the caller owns (allocated with
+ *    cudaMalloc, torch, ...) on the current device. They must be 16-byte aligned.
+ *    Host arrays of device pointers (grads, replicas) are read during the call only.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *    stream-ordered and asynchronous unless a report is requested.
+ *  - Errors are returned as zr_status; no exception crosses the ABI. A failed call
+ *    launches nothing. zr_last_error() returns a thread-local message for the last
+ *    failure on the calling thread. An asynchronous CUDA error from an earlier
+ *    launch surfaces as ZR_ERR_CUDA on a later call that synchronises.
+ *  - Overflow (a non-finite reduced gradient) is not an error: it is reported
+ *    through the overflow flag / step report, and the update is skipped.
+ *  - 16-bit formats are IEEE binary16 (ZR_F16) and bfloat16 (ZR_BF16); fp32
+ *    arithmetic is round-to-nearest-even with no fused multiply-add, in the op
+ *    order documented at each call.
+ */
+#ifndef ZR_H
+#define ZR_H
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ZR_OK = 0,
+    ZR_ERR_INVALID = 1,     /* bad argument: null/misaligned pointer, size, W, stage, dtype */
+    ZR_ERR_UNSUPPORTED = 2, /* valid request this build does not handle */
+    ZR_ERR_CUDA = 3,        /* a CUDA runtime call failed */
+    ZR_ERR_OOM = 4,         /* the library could not allocate its own small buffers */
+    ZR_ERR_TIMEOUT = 5      /* reserved: no call waits on the device without a bound */
+} zr_status;
+
+typedef enum { ZR_F16 = 0, ZR_BF16 = 1, ZR_F32 = 2 } zr_dtype;
+
+#define ZR_MAX_W 64         /* workers per ring */
+#define ZR_MAX_REPLICAS 256 /* W * A gradient replicas per fused step */
+#define ZR_ALIGN 8          /* elements; every block and tensor starts on a multiple */
+
+/* AdamW hyperparameters (fp32 values; see zr_adamw_shard_step for the formula). */
+typedef struct { float lr, beta1, beta2, eps, weight_decay; } zr_adamw_hyper;
+
+/* Dynamic loss scaling ([P2] 核心技术 (1),(3) name it; the rule is this library's
+ * reading): a step with any non-finite reduced gradient is skipped; if `dynamic`,
+ * the scale becomes max(scale*backoff, min_scale) on a skip and scale*growth after
+ * growth_interval consecutive clean steps. With dynamic = 0 the scale never changes. */
+typedef struct {
+    float init_scale, backoff, growth, min_scale;
+    int32_t growth_interval;
+    int32_t dynamic;
+} zr_scaler_cfg;
+
+/* One gradient bucket in the flat buffer: elements [start, start+len), cut into W
+ * blocks of `chunk` elements (the last blocks may be short or empty). */
+typedef struct { int64_t start, len, chunk; } zr_bucket;
+
+/* ------------------------------------------------------------------------- */
+/* Layout                                                                     */
+/* ------------------------------------------------------------------------- */
+
+/* Elements per ring block of an n-element bucket: align * ceil(n / (align * W))
+ * ([P1] 二: each of the N blocks holds phi/N; [P3] Ring AllReduce, 阶段一). */
+int64_t zr_chunk_size(int64_t n, int W, int align);
+
+/* Reverse-order bucket builder ([P1] 二: parameters in reverse definition order,
+ * output layer first, synchronised a full bucket at a time; [P3] DDP 核心实现细节).
+ * numels[ntensors]: tensor sizes in definition order (host). Tensors are placed from
+ * the last defined to the first, each at a multiple of `align` elements; a tensor is
+ * never split; a non-empty bucket closes before a tensor that would take it past
+ * cap_elems, so a tensor larger than the cap sits alone. Buckets are contiguous.
+ * out: caller array of at least ntensors entries (host); *nbuckets: count written;
+ * tensor_offsets[ntensors]: flat offset of each tensor (host, may be NULL).
+ * Errors: ZR_ERR_INVALID for null out/nbuckets, ntensors < 0, a negative numel,
+ * cap_elems < 1, W outside [1, ZR_MAX_W], align < 1. */
+zr_status zr_bucket_plan(const int64_t* numels, int ntensors, int64_t cap_elems, int W, int align,
+                         zr_bucket* out, int* nbuckets, int64_t* tensor_offsets);
+
+/* ------------------------------------------------------------------------- */
+/* Standalone collectives and optimizer (the unfused chain)                    */
+/* ------------------------------------------------------------------------- */
+
+/* Ring reduce-scatter of one n-element bucket over W workers ([P1] 二 scatter reduce,
+ * GPU0/GPU1/GPU2 example; [P3] Ring AllReduce 阶段一).
+ * grads[W]: host array of device pointers, worker w's n gradients of type dt (F16 or
+ * BF16). order[W]: host array, order[p] = worker at ring position p (NULL = identity).
+ * With C = zr_chunk_size(n, W, ZR_ALIGN), block c = [c*C, min((c+1)*C, n)) starts at
+ * position c and travels the ring; the result is
+ *     sums[i] = (((x_{order[c]}[i] + x_{order[c+1]}[i]) + ...) + x_{order[c+W-1]}[i])
+ * (positions mod W, each value converted exactly to fp32, fp32 adds left to right),
+ * which ring position (c-1) mod W owns. sums: device, n fp32 (the owners' shards in
+ * place). overflow: device int32, set to 1 (never cleared) if any sum is not finite.
+ * Errors: ZR_ERR_INVALID for n < 0, W outside [1, ZR_MAX_W], a bad order
+ * permutation, null or misaligned pointers, dt not F16/BF16. n == 0 is a no-op. */
+zr_status zr_reduce_scatter(const void* const* grads, zr_dtype dt, int64_t n, int W, const int* order,
+                            float* sums, int32_t* overflow, void* stream);
+
+/* Owner-side update of one shard ([P1] 三: average, convert to FP32 and scale, update
+ * m and v, then the FP32 master; [P3] memory table: master, m, v in FP32).
+ * Runs two kernels: a pass that sets *overflow to 1 if any shard_sums value is not
+ * finite, then, only if *overflow is 0 (read on the device), the AdamW update in place:
+ *   g = sums * r,  r = fp32(1 / (loss_scale * W)) formed in double
+ *   m = b1*m + (1-b1)*g ;  v = b2*v + (1-b2)*(g*g)
+ *   u = (m / bc1) / (sqrt(v / bc2) + eps),  bc_i = fp32(1 - beta_i^t), beta_i^t a
+ *       running product of t double multiplications
+ *   master = master*(1 - lr*wd) - lr*u     (1-b1, 1-b2, 1-lr*wd formed in fp32)
+ * t: the 1-based index of this update. All arrays: device fp32, len elements.
+ * Errors: ZR_ERR_INVALID for len < 0, t < 1, W < 1, loss_scale <= 0 or not finite,
+ * null h, null or misaligned pointers. len == 0 only runs nothing. */
+zr_status zr_adamw_shard_step(const float* shard_sums, float* m, float* v, float* master, int64_t len,
+                              const zr_adamw_hyper* h, float loss_scale, int W, int64_t t,
+                              int32_t* overflow, void* stream);
+
+/* All-gather of the updated parameters ([P1] 二 all-gather phase and 三 parameter
+ * broadcast; [P3] ZeRO stage 1 step 4): every worker ends with every block, so each of
+ * the n_replicas outputs receives round-to-nearest-even out_dt(master[i]) for all i.
+ * master: device fp32[n]; replicas: host array of n_replicas device pointers of n
+ * out_dt values. The ring hop schedule is traffic only (zr_ring_traffic).
+ * Errors: ZR_ERR_INVALID for n < 0, n_replicas outside [1, ZR_MAX_REPLICAS],
+ * out_dt not F16/BF16, null or misaligned pointers. */
+zr_status zr_all_gather(const float* master, int64_t n, zr_dtype out_dt, void* const* replicas, int n_replicas,
+                        void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* The fused step                                                              */
+/* ------------------------------------------------------------------------- */
+
+typedef struct zr_plan zr_plan;
+
+typedef struct {
+    int32_t W;                /* workers, 1..ZR_MAX_W */
+    int32_t A;                /* micro-batches per worker, W*A <= ZR_MAX_REPLICAS */
+    zr_dtype dtype;           /* gradient and parameter type: ZR_F16 or ZR_BF16 */
+    int32_t stage;            /* ZeRO stage 1, 2 or 3 (memory plan; same arithmetic) */
+    int32_t align;            /* tensor alignment in elements; must be ZR_ALIGN */
+    int64_t cap;              /* bucket cap in elements */
+    int32_t ntensors;
+    const int64_t* numels;    /* host, definition order */
+    const int32_t* order;     /* host [W] ring order, NULL = identity */
+    zr_scaler_cfg scaler;
+} zr_plan_desc;
+
+/* Optimizer state and parameter replica, two sets (ping-pong), in the flat layout of
+ * zr_plan_numel elements. Set k (k = the plan's current index, 0 after create/reset)
+ * holds the live values; a step reads set k and writes set 1-k, and the index flips
+ * only if the step was clean, so a skipped step leaves set k bit-unchanged.
+ * All device pointers; param is of the plan's dtype. */
+typedef struct {
+    float* master[2];
+    float* m[2];
+    float* v[2];
+    void* param[2];
+} zr_state;
+
+typedef struct {
+    int32_t overflow;      /* the last step saw a non-finite reduced gradient */
+    int32_t skipped;       /* ... and was therefore skipped */
+    int32_t current;       /* index of the live state set after the last step */
+    int32_t stage;
+    float scale_used;      /* loss scale of the last step */
+    float scale;           /* loss scale for the next step */
+    int64_t t;             /* committed AdamW updates */
+    int64_t steps;         /* steps run, skipped included */
+    int64_t skipped_total;
+    int64_t good;          /* clean steps since the last scale change */
+    int64_t n_real;        /* parameters (sum of numels) */
+    int64_t bytes_alg;     /* algorithmic HBM bytes of one step: (2*W*A + 26) * n_real */
+} zr_step_report;
+
+/* Builds the bucket table, the tile schedule and the device control block.
+ * *out receives the plan (free with zr_plan_destroy). The control block starts with
+ * k = 0, t = 0, scale = scaler.init_scale.
+ * Errors: ZR_ERR_INVALID (see zr_plan_desc), ZR_ERR_OOM, ZR_ERR_CUDA. */
+zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out);
+zr_status zr_plan_destroy(zr_plan* p);
+int64_t zr_plan_numel(const zr_plan* p);          /* flat elements per replica and state array */
+int32_t zr_plan_nbuckets(const zr_plan* p);
+/* Copies the bucket table (nbuckets entries) and tensor offsets (ntensors) to host arrays. */
+zr_status zr_plan_buckets(const zr_plan* p, zr_bucket* buckets, int64_t* tensor_offsets);
+/* Resets the control block (k = 0, t = 0, scale) on `stream`. */
+zr_status zr_plan_reset(zr_plan* p, void* stream);
+
+/* One fused step, one kernel launch: for every element of every bucket, the ring-order
+ * fp32 sum of the W workers' values, each worker's value being the fp32 sum of its A
+ * micro-batch gradients in micro-batch order ([P3] Gradient Accumulation); then the
+ * unscale and mean, the overflow flag, AdamW and the 16-bit cast exactly as
+ * zr_reduce_scatter + zr_adamw_shard_step + zr_all_gather, reading state set k and
+ * writing set 1-k. The last block to finish ORs all flags and applies the loss-scale
+ * rule; on a clean step it sets t += 1 and k = 1-k ([P2] 核心技术 (3) dynamic scaling).
+ * stage must be 1, 2 or 3 ([P3] ZeRO stages; [P2] (11)-(13)): the stages share this
+ * arithmetic and differ in what a real worker keeps resident.
+ * grads[W*A]: host array of device pointers; replica w*A + a is worker w's micro-batch
+ * a, zr_plan_numel elements of the plan's dtype. rep: NULL for a fully asynchronous
+ * call; otherwise the call synchronises `stream` and fills *rep.
+ * Errors: ZR_ERR_INVALID for a null plan/state/hyper, stage outside 1..3, null or
+ * misaligned pointers, aliasing of the two state sets; ZR_ERR_CUDA. */
+zr_status zr_step(zr_plan* p, int stage, const void* const* grads, const zr_state* st,
+                  const zr_adamw_hyper* h, void* stream, zr_step_report* rep);
+
+/* As zr_step, with the gradients in HOST memory: copies host_grads[r] (pinned host
+ * memory gives full speed) into the device buffers dev_grads[r] with one
+ * cudaMemcpyAsync per replica and bucket, launches the step, and reads the report
+ * back (rep is required). Bucket b's copies are issued in bucket order. */
+zr_status zr_step_from_host(zr_plan* p, int stage, const void* const* host_grads, void* const* dev_grads,
+                            const zr_state* st, const zr_adamw_hyper* h, void* stream, zr_step_report* rep);
+
+/* Synchronises `stream` and reads the control block into *rep. */
+zr_status zr_plan_report(zr_plan* p, void* stream, zr_step_report* rep);
+
+/* ------------------------------------------------------------------------- */
+/* Accounting                                                                 */
+/* ------------------------------------------------------------------------- */
+
+/* Model-state bytes per worker under mixed precision + Adam ([P3] memory table and
+ * ZeRO formulas; [P1] 三/四 "2+2+K", K = 12): stage 0 (DDP) 16n; stage 1
+ * 4n + 12n/W; stage 2 2n + 14n/W; stage 3 16n/W (integer division). -1 on bad input. */
+int64_t zr_model_state_bytes(int stage, int64_t n, int W);
+
+/* Elements each ring position sends and receives in one phase over an n-element
+ * bucket ([P1] 二 traffic: (N-1) * phi / N per phase when N divides phi; [P3]
+ * 通信量分析). Position p sends every block but (p+1) mod W in reduce-scatter and
+ * every block but (p+2) mod W in all-gather; it receives every block but p, resp.
+ * (p+1) mod W. Arrays are host [W]; any may be NULL. */
+zr_status zr_ring_traffic(int64_t n, int W, int align, int64_t* rs_sent, int64_t* rs_recv, int64_t* ag_sent,
+                          int64_t* ag_recv);
+
+const char* zr_status_str(zr_status s);
+const char* zr_last_error(void);
+/* Library version string. */
+const char* zr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

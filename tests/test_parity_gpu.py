@@ -1,0 +1,377 @@
+"""GPU parity: every C-ABI call against the oracle, element by element, on seeded inputs.
+
+Bar (BASELINE tolerances): reduced sums, overflow flag and skip decision bit-exact; fp32 master/m/v
+within 2 ulp; 16-bit params within 1 ulp. The kernels follow the oracle's op order with IEEE
+round-to-nearest ops and no contraction, so these tests also assert bit-exactness where it is expected.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zero_gradient_reduction_gb300 as zr
+import zrgen
+from _harness import Layout
+
+pytestmark = pytest.mark.gpu
+
+F32 = np.float32
+HYPER = zr.AdamW(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+OHYPER = oracle.AdamW(1e-3, 0.9, 0.999, 1e-8, 0.01)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.empty_cache()
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f32bits(t) -> np.ndarray:
+    a = t.detach().cpu().numpy() if isinstance(t, torch.Tensor) else t
+    return np.ascontiguousarray(a, dtype=F32).view(np.uint32)
+
+
+def to_dev16(a: np.ndarray, dtype: int) -> torch.Tensor:
+    tdt = torch.float16 if dtype == zr.F16 else torch.bfloat16
+    return torch.from_numpy(a.view(np.int16).copy()).cuda().view(tdt)
+
+
+def ulp_diff_f32(a: np.ndarray, b: np.ndarray) -> int:
+    """Max distance in representable fp32 steps (sign-magnitude order)."""
+    ia = np.asarray(a, F32).view(np.int32).astype(np.int64)
+    ib = np.asarray(b, F32).view(np.int32).astype(np.int64)
+    ia = np.where(ia < 0, -(ia & 0x7FFFFFFF), ia)
+    ib = np.where(ib < 0, -(ib & 0x7FFFFFFF), ib)
+    return int(np.max(np.abs(ia - ib))) if ia.size else 0
+
+
+def ulp_diff_16(a: np.ndarray, b: np.ndarray) -> int:
+    ia = np.asarray(a, np.uint16).astype(np.int64)
+    ib = np.asarray(b, np.uint16).astype(np.int64)
+    ia = np.where(ia & 0x8000, -(ia & 0x7FFF), ia)
+    ib = np.where(ib & 0x8000, -(ib & 0x7FFF), ib)
+    return int(np.max(np.abs(ia - ib))) if ia.size else 0
+
+
+def assert_state_close(gm, gmm, gv, gp, om, omm, ov, op, exact=True, where=""):
+    for name, g, o in (("master", gm, om), ("m", gmm, omm), ("v", gv, ov)):
+        d = ulp_diff_f32(g, o)
+        assert d <= 2, f"{where}{name}: {d} ulp"
+        if exact:
+            assert np.array_equal(np.asarray(g, F32).view(np.uint32), np.asarray(o, F32).view(np.uint32)), \
+                f"{where}{name}: not bit-exact ({d} ulp)"
+    d = ulp_diff_16(gp, op)
+    assert d <= 1, f"{where}param: {d} ulp"
+    if exact:
+        assert np.array_equal(gp, op), f"{where}param: not bit-exact"
+
+
+# ----------------------------------------------------------------------------- generator
+@pytest.mark.parametrize("dt", [zrgen.F16, zrgen.BF16, zrgen.F32])
+def test_generator_host_equals_device(dt):
+    table = torch.from_numpy(zrgen.normal_table().copy()).cuda()
+    for first, n, scale in ((0, 1, 1.0), (3, 1001, 0.5), (8, 65536, 655.36), (12345, 300_001, 1e-4)):
+        host = zrgen.fill_host(n, dt, 7, 99, first, scale)
+        tdt = {zrgen.F16: torch.float16, zrgen.BF16: torch.bfloat16, zrgen.F32: torch.float32}[dt]
+        buf = torch.empty(n, dtype=tdt, device="cuda")
+        zrgen.fill_dev(buf.data_ptr(), n, dt, 7, 99, first, scale, table.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        devb = u16(buf) if dt != zrgen.F32 else buf.cpu().numpy().view(np.uint32)
+        hostb = host if dt != zrgen.F32 else host.view(np.uint32)
+        assert np.array_equal(devb, hostb)
+
+
+# ----------------------------------------------------------------------------- reduce-scatter
+def _rand_grads(rng, W, n, dtype, scale=3.0):
+    out = []
+    for _ in range(W):
+        out.append(oracle.encode(dtype, (rng.normal(size=n) * scale).astype(F32)))
+    return out
+
+
+def _oracle_sums(grads, W, n, dtype, order):
+    C = oracle.chunk_size(n, W, 8)
+    z = np.zeros(n, F32)
+    rep, sums = oracle.step(W, 1, dtype, np.array([[0, n, C]]), grads, z.copy(), z.copy(), z.copy(),
+                            np.zeros(n, np.uint16), OHYPER, oracle.new_scaler(), order=order, want_sums=True)
+    return sums, rep.overflow
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 8, 9, 16])
+@pytest.mark.parametrize("dtype", [zr.F16, zr.BF16])
+def test_reduce_scatter_bit_exact(W, dtype):
+    rng = np.random.default_rng(W * 10 + dtype)
+    for n in (1, 7, 8, 100, 8 * W * 3 + 3, 65_541, 300_000):
+        order = list(rng.permutation(W))
+        grads = _rand_grads(rng, W, n, dtype)
+        want, flag = _oracle_sums(grads, W, n, dtype, order)
+        gd = [to_dev16(g, dtype) for g in grads]
+        sums = torch.empty(n, dtype=torch.float32, device="cuda")
+        of = torch.zeros(1, dtype=torch.int32, device="cuda")
+        zr.reduce_scatter(gd, sums, of, order=order)
+        torch.cuda.synchronize()
+        assert np.array_equal(f32bits(sums), want.view(np.uint32)), (W, n)
+        assert int(of.item()) == flag == 0
+
+
+def test_reduce_scatter_overflow_flag_sticky():
+    rng = np.random.default_rng(1)
+    W, n = 4, 10_000
+    grads = _rand_grads(rng, W, n, zr.F16)
+    of = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sums = torch.empty(n, dtype=torch.float32, device="cuda")
+    zr.reduce_scatter([to_dev16(g, zr.F16) for g in grads], sums, of)
+    torch.cuda.synchronize()
+    assert of.item() == 0
+    for bad, pos in ((0x7C00, 9_999), (0x7E00, 5), (0xFC00, 4_321)):
+        g2 = [g.copy() for g in grads]
+        g2[2][pos] = bad
+        want, flag = _oracle_sums(g2, W, n, zr.F16, None)
+        of.zero_()
+        zr.reduce_scatter([to_dev16(g, zr.F16) for g in g2], sums, of)
+        torch.cuda.synchronize()
+        assert of.item() == 1 == flag
+        got = sums.cpu().numpy()
+        assert np.array_equal(np.isnan(got), np.isnan(want))
+        fin = np.isfinite(want)
+        assert np.array_equal(got[fin].view(np.uint32), want[fin].view(np.uint32))
+        # the flag is never cleared by a clean call
+        zr.reduce_scatter([to_dev16(g, zr.F16) for g in grads], sums, of)
+        torch.cuda.synchronize()
+        assert of.item() == 1
+
+
+# ----------------------------------------------------------------------------- AdamW shard step
+@pytest.mark.parametrize("n", [1, 5, 4096, 100_003])
+@pytest.mark.parametrize("t", [1, 7])
+def test_adamw_shard_step_bit_exact(n, t):
+    rng = np.random.default_rng(n + t)
+    S, W = 1024.0, 3
+    sums = (rng.normal(size=n) * 30.0).astype(F32)
+    m = (rng.normal(size=n) * 1e-3).astype(F32)
+    v = np.abs(rng.normal(size=n) * 1e-5).astype(F32)
+    p = (rng.normal(size=n) * 0.02).astype(F32)
+    dsums, dm, dv, dp = (torch.from_numpy(x.copy()).cuda() for x in (sums, m, v, p))
+    of = torch.zeros(1, dtype=torch.int32, device="cuda")
+    zr.adamw_shard_step(dsums, dm, dv, dp, HYPER, S, W, t, of)
+    torch.cuda.synchronize()
+    g = (sums * oracle.unscale_factor(S, W)).astype(F32)
+    oracle.adamw(g, p, m, v, OHYPER, oracle.bias_correction(0.9, t), oracle.bias_correction(0.999, t))
+    assert of.item() == 0
+    for dev, host in ((dp, p), (dm, m), (dv, v)):
+        assert np.array_equal(f32bits(dev), host.view(np.uint32))
+
+
+def test_adamw_shard_step_skips_on_flag():
+    rng = np.random.default_rng(3)
+    n = 1000
+    sums = (rng.normal(size=n)).astype(F32)
+    arrs = [(rng.normal(size=n)).astype(F32) for _ in range(3)]
+    arrs[1] = np.abs(arrs[1])
+    dev = [torch.from_numpy(a.copy()).cuda() for a in arrs]
+    # preset flag: no update
+    of = torch.ones(1, dtype=torch.int32, device="cuda")
+    zr.adamw_shard_step(torch.from_numpy(sums).cuda(), dev[0], dev[1], dev[2], HYPER, 1.0, 1, 1, of)
+    torch.cuda.synchronize()
+    for d, a in zip(dev, arrs):
+        assert np.array_equal(f32bits(d), a.view(np.uint32))
+    # non-finite shard value: the flag pass sets the flag and the update is skipped
+    sums[777] = np.inf
+    of.zero_()
+    zr.adamw_shard_step(torch.from_numpy(sums).cuda(), dev[0], dev[1], dev[2], HYPER, 1.0, 1, 1, of)
+    torch.cuda.synchronize()
+    assert of.item() == 1
+    for d, a in zip(dev, arrs):
+        assert np.array_equal(f32bits(d), a.view(np.uint32))
+
+
+# ----------------------------------------------------------------------------- all-gather
+@pytest.mark.parametrize("dtype", [zr.F16, zr.BF16])
+@pytest.mark.parametrize("R", [1, 3, 8])
+def test_all_gather_bit_exact(dtype, R):
+    rng = np.random.default_rng(R)
+    n = 50_007
+    x = (rng.normal(size=n) * rng.choice([1e-9, 1e-6, 1e-2, 1.0, 1e4, 7e4], size=n)).astype(F32)
+    x[:6] = [0.0, -0.0, np.inf, -np.inf, 65519.0, 65520.0]
+    want = oracle.encode(dtype, x)
+    tdt = torch.float16 if dtype == zr.F16 else torch.bfloat16
+    reps = [torch.empty(n, dtype=tdt, device="cuda") for _ in range(R)]
+    zr.all_gather(torch.from_numpy(x).cuda(), reps)
+    torch.cuda.synchronize()
+    for r in reps:
+        assert np.array_equal(u16(r), want)
+
+
+# ----------------------------------------------------------------------------- fused step
+class FusedRun:
+    """A fused-step run on the GPU with the full oracle beside it (small sizes)."""
+
+    def __init__(self, numels, W, A, dtype, cap, S, dynamic=False, order=None, seed=0, sigma=None, stage=2,
+                 interval=1000):
+        self.plan = zr.Plan(numels, W=W, A=A, dtype=dtype, stage=stage, cap=cap, order=order,
+                            scaler=zr.Scaler(S, dynamic, growth_interval=interval))
+        self.W, self.A, self.dtype, self.order = W, A, dtype, order
+        sig = np.full(len(numels), 1e-2, F32) if sigma is None else np.asarray(sigma, F32)
+        self.layout = Layout(numels, self.plan.tensor_offsets, sig, seed, dtype)
+        n = self.plan.numel
+        self.n = n
+        self.table = torch.from_numpy(zrgen.normal_table().copy()).cuda()
+        self.state = self.plan.new_state()
+        self.state.master[0].zero_()
+        self.layout.master_dev(self.state.master[0], self.table, torch.cuda.current_stream().cuda_stream)
+        zr.all_gather(self.state.master[0], [self.state.param[0]])
+        self.grads = [torch.zeros(n, dtype=self.plan.torch_dtype(), device="cuda") for _ in range(W * A)]
+        om = self.layout.master_host(0, n)
+        self.o = [om, np.zeros(n, F32), np.zeros(n, F32), oracle.encode(dtype, om)]
+        self.osc = oracle.new_scaler(S, dynamic, interval=interval)
+        self.S = S
+        self.current = 0
+
+    def step(self, step, inject=None, stage=None):
+        st = torch.cuda.current_stream().cuda_stream
+        S = self.S
+        ograds = []
+        for r in range(self.W * self.A):
+            self.layout.grads_dev(self.grads[r], step, r, S, self.table, st)
+            ograds.append(self.layout.grads_host(0, self.n, step, r, S))
+        if inject is not None:
+            r, i = inject
+            bits = 0x7C00 if self.dtype == zr.F16 else 0x7F80
+            self.grads[r].view(torch.int16)[i] = np.int16(np.uint16(bits).view(np.int16))
+            ograds[r][i] = bits
+        rep = self.plan.step(self.grads, self.state, HYPER, stage=stage, report=True)
+        orep, _ = oracle.step(self.W, self.A, self.dtype, self.plan.buckets, ograds, *self.o, OHYPER, self.osc,
+                              order=self.order)
+        assert rep.overflow == orep.overflow and rep.skipped == orep.skipped
+        assert rep.scale_used == orep.scale_used and rep.scale == orep.scale_next
+        assert rep.t == orep.t_after
+        self.S = rep.scale
+        self.current = rep.current
+        return rep, orep
+
+    def live(self):
+        L = self.state.live(self.current)
+        return (L["master"].cpu().numpy(), L["m"].cpu().numpy(), L["v"].cpu().numpy(), u16(L["param"]))
+
+    def check(self, where=""):
+        assert_state_close(*self.live(), *self.o, exact=True, where=where)
+
+
+def test_fused_tiny_config_bit_exact():
+    """flat n = 786,432, W = 3, fp16, one bucket, S = 1024 static, 3 steps, seed 0."""
+    w = zrgen.workload("tiny")
+    run = FusedRun(list(w.tensors), w.W, w.A, w.dtype, w.cap, w.init_scale, w.dynamic, seed=w.seed,
+                   sigma=zrgen.sigma_per_tensor(w), stage=w.stage)
+    assert len(run.plan.buckets) == 1 and run.plan.numel == 786_432
+    for s in range(1, w.steps + 1):
+        rep, orep = run.step(s)
+        assert rep.overflow == 0 and rep.current == s % 2 and rep.t == s
+        run.check(f"step {s}: ")
+
+
+@pytest.mark.parametrize("W,A,dtype", [(2, 1, zr.F16), (3, 1, zr.BF16), (5, 1, zr.F16), (8, 1, zr.BF16),
+                                       (2, 4, zr.BF16), (4, 4, zr.F16), (8, 4, zr.BF16), (3, 3, zr.BF16),
+                                       (16, 1, zr.F16)])
+def test_fused_ragged_buckets(W, A, dtype):
+    rng = np.random.default_rng(W * 100 + A)
+    numels = [1000, 37, 5000, 8, 123_457, 64, 9_999, 3, 40_000]
+    order = list(rng.permutation(W))
+    run = FusedRun(numels, W, A, dtype, cap=20_000, S=8.0, order=order, seed=3,
+                   sigma=rng.uniform(1e-3, 1e-1, size=len(numels)))
+    assert len(run.plan.buckets) >= 4
+    for s in range(1, 4):
+        run.step(s)
+        run.check(f"W={W} A={A} step {s}: ")
+
+
+def test_fused_skip_then_resume():
+    numels = [20_000, 4_000, 30_000]
+    run = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=5)
+    run.step(1)
+    before = [x.copy() for x in run.live()]
+    cur = run.current
+    rep, orep = run.step(2, inject=(1, int(run.plan.tensor_offsets[2]) + 123))
+    assert rep.overflow == 1 and rep.skipped == 1 and rep.current == cur and rep.t == 1
+    assert rep.scale == 32768.0 and rep.skipped_total == 1
+    after = run.live()
+    for a, b in zip(after, before):
+        assert a.tobytes() == b.tobytes()
+    for s in (3, 4):
+        run.step(s)
+        run.check(f"resume step {s}: ")
+
+
+def test_fused_scale_growth():
+    run = FusedRun([4096, 1000], 2, 1, zr.BF16, cap=10_000, S=4.0, dynamic=True, interval=2)
+    scales = []
+    for s in range(1, 6):
+        rep, _ = run.step(s)
+        scales.append(rep.scale_used)
+    assert scales == [4.0, 4.0, 8.0, 8.0, 16.0]
+    run.check()
+
+
+def test_stages_identical():
+    outs = []
+    for stage in (1, 2, 3):
+        run = FusedRun([70_000, 5000], 4, 1, zr.BF16, cap=50_000, S=1.0, seed=11, stage=stage)
+        for s in (1, 2):
+            rep, _ = run.step(s, stage=stage)
+            assert rep.stage == stage
+        outs.append([x.tobytes() for x in run.live()])
+    assert outs[0] == outs[1] == outs[2]
+
+
+def test_step_from_host_equals_step():
+    numels = [50_000, 777, 12_345]
+    a = FusedRun(numels, 3, 1, zr.F16, cap=40_000, S=1024.0, seed=2)
+    b = FusedRun(numels, 3, 1, zr.F16, cap=40_000, S=1024.0, seed=2)
+    for s in (1, 2):
+        a.step(s)
+        host = []
+        for r in range(3):
+            h = torch.from_numpy(b.layout.grads_host(0, b.n, s, r, b.S).view(np.int16).copy()).pin_memory()
+            host.append(h)
+        rep = b.plan.step_from_host(host, b.grads, b.state, HYPER)
+        assert rep.t == s and rep.overflow == 0
+        b.current = rep.current
+        for x, y in zip(a.live(), b.live()):
+            assert x.tobytes() == y.tobytes()
+
+
+def test_error_paths():
+    plan = zr.Plan([1024], W=2, A=1, dtype=zr.BF16, stage=2, cap=2048)
+    st = plan.new_state()
+    grads = [torch.zeros(plan.numel, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    with pytest.raises(zr.ZrError) as e:
+        plan.step(grads, st, HYPER, stage=4)
+    assert e.value.status == 1
+    with pytest.raises(zr.ZrError):
+        plan.step([grads[0], grads[1][1:]], st, HYPER)  # 2-byte offset: misaligned
+    st.master[1] = st.master[0]
+    with pytest.raises(zr.ZrError):
+        plan.step(grads, st, HYPER)
+    with pytest.raises(zr.ZrError):
+        zr.Plan([8], W=65, A=1)
+    with pytest.raises(zr.ZrError):
+        zr.Plan([8], W=8, A=33)
+    with pytest.raises(zr.ZrError):
+        zr.reduce_scatter(grads, torch.empty(1024, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda"),
+                          order=[0, 0])
+    # nothing above launched: the library still works
+    plan.reset()
+    st2 = plan.new_state()
+    st2.master[0].zero_()
+    r = plan.step(grads, st2, HYPER, report=True)
+    assert r.t == 1 and r.overflow == 0

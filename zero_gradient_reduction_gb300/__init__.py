@@ -1,0 +1,331 @@
+"""Python binding of libzr, the GB300-native post-backward ZeRO step (C ABI in include/zr.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA kernels.
+PyTorch supplies device memory and streams. If libzr.so is missing this module raises
+on import of the library (there is no fallback of any kind).
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libzr.so")
+
+F16, BF16, F32 = 0, 1, 2
+MAX_W, MAX_REPLICAS, ALIGN = 64, 256, 8
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "out of memory", 5: "timeout"}
+
+
+class ZrError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class Bucket(ctypes.Structure):
+    _fields_ = [("start", ctypes.c_int64), ("len", ctypes.c_int64), ("chunk", ctypes.c_int64)]
+
+
+class Hyper(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float)]
+
+
+class ScalerCfg(ctypes.Structure):
+    _fields_ = [("init_scale", ctypes.c_float), ("backoff", ctypes.c_float), ("growth", ctypes.c_float),
+                ("min_scale", ctypes.c_float), ("growth_interval", ctypes.c_int32), ("dynamic", ctypes.c_int32)]
+
+
+class PlanDesc(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_int32), ("A", ctypes.c_int32), ("dtype", ctypes.c_int), ("stage", ctypes.c_int32),
+                ("align", ctypes.c_int32), ("cap", ctypes.c_int64), ("ntensors", ctypes.c_int32),
+                ("numels", ctypes.POINTER(ctypes.c_int64)), ("order", ctypes.POINTER(ctypes.c_int32)),
+                ("scaler", ScalerCfg)]
+
+
+class StateC(ctypes.Structure):
+    _fields_ = [("master", ctypes.c_void_p * 2), ("m", ctypes.c_void_p * 2), ("v", ctypes.c_void_p * 2),
+                ("param", ctypes.c_void_p * 2)]
+
+
+class StepReport(ctypes.Structure):
+    _fields_ = [("overflow", ctypes.c_int32), ("skipped", ctypes.c_int32), ("current", ctypes.c_int32),
+                ("stage", ctypes.c_int32), ("scale_used", ctypes.c_float), ("scale", ctypes.c_float),
+                ("t", ctypes.c_int64), ("steps", ctypes.c_int64), ("skipped_total", ctypes.c_int64),
+                ("good", ctypes.c_int64), ("n_real", ctypes.c_int64), ("bytes_alg", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """The loaded libzr (ctypes). Raises if the library has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"libzr.so not found at {LIB_PATH}; build it with __graft_entry__.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i64, i32, st = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int
+            sig = {
+                "zr_chunk_size": (i64, [i64, i32, i32]),
+                "zr_bucket_plan": (st, [vp, i32, i64, i32, i32, vp, ctypes.POINTER(ctypes.c_int), vp]),
+                "zr_reduce_scatter": (st, [vp, i32, i64, i32, vp, vp, vp, vp]),
+                "zr_adamw_shard_step": (st, [vp, vp, vp, vp, i64, ctypes.POINTER(Hyper), ctypes.c_float, i32, i64,
+                                             vp, vp]),
+                "zr_all_gather": (st, [vp, i64, i32, vp, i32, vp]),
+                "zr_plan_create": (st, [ctypes.POINTER(PlanDesc), ctypes.POINTER(vp)]),
+                "zr_plan_destroy": (st, [vp]),
+                "zr_plan_numel": (i64, [vp]),
+                "zr_plan_nbuckets": (ctypes.c_int32, [vp]),
+                "zr_plan_buckets": (st, [vp, vp, vp]),
+                "zr_plan_reset": (st, [vp, vp]),
+                "zr_step": (st, [vp, i32, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp,
+                                 ctypes.POINTER(StepReport)]),
+                "zr_step_from_host": (st, [vp, i32, vp, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp,
+                                           ctypes.POINTER(StepReport)]),
+                "zr_plan_report": (st, [vp, vp, ctypes.POINTER(StepReport)]),
+                "zr_model_state_bytes": (i64, [i32, i64, i32]),
+                "zr_ring_traffic": (st, [i64, i32, i32, vp, vp, vp, vp]),
+                "zr_status_str": (ctypes.c_char_p, [st]),
+                "zr_last_error": (ctypes.c_char_p, []),
+                "zr_version": (ctypes.c_char_p, []),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise ZrError(status, lib().zr_last_error().decode(errors="replace"))
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t) -> int:
+    return int(t.data_ptr())
+
+
+def _ptr_array(tensors) -> ctypes.Array:
+    return (ctypes.c_void_p * len(tensors))(*[_ptr(t) for t in tensors])
+
+
+def _host_ptr_array(arrays) -> ctypes.Array:
+    ptrs = []
+    for a in arrays:
+        ptrs.append(a.ctypes.data if isinstance(a, np.ndarray) else int(a.data_ptr()))
+    return (ctypes.c_void_p * len(ptrs))(*ptrs)
+
+
+# ----------------------------------------------------------------------------- layout and accounting
+def chunk_size(n: int, W: int, align: int = ALIGN) -> int:
+    return int(lib().zr_chunk_size(int(n), int(W), int(align)))
+
+
+def bucket_plan(numels: Sequence[int], cap: int, W: int, align: int = ALIGN):
+    """(buckets int64 [nb, 3] of (start, len, chunk), tensor_offsets int64 [ntensors])."""
+    nt = len(numels)
+    num = np.ascontiguousarray(np.asarray(numels, dtype=np.int64))
+    out = (Bucket * max(nt, 1))()
+    offs = np.zeros(max(nt, 1), dtype=np.int64)
+    nb = ctypes.c_int(0)
+    _check(lib().zr_bucket_plan(num.ctypes.data if nt else None, nt, int(cap), int(W), int(align),
+                                ctypes.addressof(out), ctypes.byref(nb), offs.ctypes.data))
+    b = np.array([[out[i].start, out[i].len, out[i].chunk] for i in range(nb.value)], dtype=np.int64).reshape(-1, 3)
+    return b, offs[:nt]
+
+
+def model_state_bytes(stage: int, n: int, W: int) -> int:
+    return int(lib().zr_model_state_bytes(int(stage), int(n), int(W)))
+
+
+def ring_traffic(n: int, W: int, align: int = ALIGN):
+    arrs = [np.zeros(W, dtype=np.int64) for _ in range(4)]
+    _check(lib().zr_ring_traffic(int(n), int(W), int(align), *[a.ctypes.data for a in arrs]))
+    return dict(zip(("rs_sent", "rs_recv", "ag_sent", "ag_recv"), arrs))
+
+
+# ----------------------------------------------------------------------------- standalone collectives
+@dataclasses.dataclass
+class AdamW:
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.01
+
+    def c(self) -> Hyper:
+        return Hyper(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay)
+
+
+def _dt_of(t) -> int:
+    import torch
+    return {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32}[t.dtype]
+
+
+def reduce_scatter(grads: Sequence, sums, overflow, order: Optional[Sequence[int]] = None, n: Optional[int] = None,
+                   stream=None) -> None:
+    """Ring reduce-scatter of W device gradient tensors (fp16/bf16) into fp32 `sums` (see zr_reduce_scatter)."""
+    W = len(grads)
+    n = int(grads[0].numel()) if n is None else int(n)
+    ordc = (ctypes.c_int * W)(*order) if order is not None else None
+    arr = _ptr_array(grads)  # must outlive the call
+    _check(lib().zr_reduce_scatter(ctypes.addressof(arr), _dt_of(grads[0]), n, W,
+                                   ctypes.addressof(ordc) if ordc is not None else None, _ptr(sums), _ptr(overflow),
+                                   _stream_handle(stream)))
+
+
+def adamw_shard_step(shard_sums, m, v, master, hyper: AdamW, loss_scale: float, W: int, t: int, overflow,
+                     length: Optional[int] = None, stream=None) -> None:
+    n = int(master.numel()) if length is None else int(length)
+    h = hyper.c()
+    _check(lib().zr_adamw_shard_step(_ptr(shard_sums), _ptr(m), _ptr(v), _ptr(master), n, ctypes.byref(h),
+                                     float(loss_scale), int(W), int(t), _ptr(overflow), _stream_handle(stream)))
+
+
+def all_gather(master, replicas: Sequence, n: Optional[int] = None, stream=None) -> None:
+    n = int(master.numel()) if n is None else int(n)
+    arr = _ptr_array(replicas)
+    _check(lib().zr_all_gather(_ptr(master), n, _dt_of(replicas[0]), ctypes.addressof(arr), len(replicas),
+                               _stream_handle(stream)))
+
+
+# ----------------------------------------------------------------------------- fused step
+@dataclasses.dataclass
+class Scaler:
+    init_scale: float = 1.0
+    dynamic: bool = False
+    backoff: float = 0.5
+    growth: float = 2.0
+    min_scale: float = 1.0
+    growth_interval: int = 1000
+
+    def c(self) -> ScalerCfg:
+        return ScalerCfg(self.init_scale, self.backoff, self.growth, self.min_scale, self.growth_interval,
+                         1 if self.dynamic else 0)
+
+
+class State:
+    """The two (ping-pong) sets of fp32 master/m/v and the 16-bit parameter replica, as torch tensors."""
+
+    def __init__(self, numel: int, dtype, device="cuda"):
+        import torch
+        self.master = [torch.empty(numel, dtype=torch.float32, device=device) for _ in range(2)]
+        self.m = [torch.zeros(numel, dtype=torch.float32, device=device) for _ in range(2)]
+        self.v = [torch.zeros(numel, dtype=torch.float32, device=device) for _ in range(2)]
+        self.param = [torch.empty(numel, dtype=dtype, device=device) for _ in range(2)]
+
+    def c(self) -> StateC:
+        s = StateC()
+        for k in range(2):
+            s.master[k] = _ptr(self.master[k])
+            s.m[k] = _ptr(self.m[k])
+            s.v[k] = _ptr(self.v[k])
+            s.param[k] = _ptr(self.param[k])
+        return s
+
+    def live(self, k: int):
+        return dict(master=self.master[k], m=self.m[k], v=self.v[k], param=self.param[k])
+
+
+class Plan:
+    """A bucketed ZeRO step over W emulated workers (zr_plan_create / zr_step)."""
+
+    def __init__(self, numels: Sequence[int], W: int, A: int = 1, dtype: int = BF16, stage: int = 2,
+                 cap: int = 25_000_000, order: Optional[Sequence[int]] = None, scaler: Scaler = Scaler()):
+        self._numels = np.ascontiguousarray(np.asarray(numels, dtype=np.int64))
+        self._order = (ctypes.c_int32 * W)(*order) if order is not None else None
+        d = PlanDesc()
+        d.W, d.A, d.dtype, d.stage, d.align, d.cap = int(W), int(A), int(dtype), int(stage), ALIGN, int(cap)
+        d.ntensors = len(self._numels)
+        d.numels = self._numels.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+        d.order = ctypes.cast(self._order, ctypes.POINTER(ctypes.c_int32)) if self._order is not None else None
+        d.scaler = scaler.c()
+        h = ctypes.c_void_p()
+        _check(lib().zr_plan_create(ctypes.byref(d), ctypes.byref(h)))
+        self._h = h
+        self.W, self.A, self.dtype, self.stage = int(W), int(A), int(dtype), int(stage)
+        self.numel = int(lib().zr_plan_numel(h))
+        nb = int(lib().zr_plan_nbuckets(h))
+        b = (Bucket * max(nb, 1))()
+        offs = np.zeros(len(self._numels), dtype=np.int64)
+        _check(lib().zr_plan_buckets(h, ctypes.addressof(b), offs.ctypes.data))
+        self.buckets = np.array([[b[i].start, b[i].len, b[i].chunk] for i in range(nb)], dtype=np.int64).reshape(-1, 3)
+        self.tensor_offsets = offs
+        self.n_real = int(self._numels.sum())
+
+    @property
+    def handle(self):
+        return self._h
+
+    def torch_dtype(self):
+        import torch
+        return torch.float16 if self.dtype == F16 else torch.bfloat16
+
+    def new_state(self, device="cuda") -> State:
+        return State(self.numel, self.torch_dtype(), device)
+
+    def step(self, grads: Sequence, state: State, hyper: AdamW, stage: Optional[int] = None, stream=None,
+             report: bool = False):
+        arr = _ptr_array(grads)
+        st = state.c()
+        h = hyper.c()
+        rep = StepReport() if report else None
+        _check(lib().zr_step(self._h, int(stage if stage is not None else self.stage), ctypes.addressof(arr),
+                             ctypes.byref(st), ctypes.byref(h), _stream_handle(stream),
+                             ctypes.byref(rep) if rep is not None else None))
+        return rep
+
+    def step_from_host(self, host_grads: Sequence, dev_grads: Sequence, state: State, hyper: AdamW,
+                       stage: Optional[int] = None, stream=None) -> StepReport:
+        ha = _host_ptr_array(host_grads)
+        da = _ptr_array(dev_grads)
+        st = state.c()
+        h = hyper.c()
+        rep = StepReport()
+        _check(lib().zr_step_from_host(self._h, int(stage if stage is not None else self.stage),
+                                       ctypes.addressof(ha), ctypes.addressof(da), ctypes.byref(st), ctypes.byref(h),
+                                       _stream_handle(stream), ctypes.byref(rep)))
+        return rep
+
+    def report(self, stream=None) -> StepReport:
+        rep = StepReport()
+        _check(lib().zr_plan_report(self._h, _stream_handle(stream), ctypes.byref(rep)))
+        return rep
+
+    def reset(self, stream=None) -> None:
+        _check(lib().zr_plan_reset(self._h, _stream_handle(stream)))
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().zr_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+__all__ = ["lib", "ZrError", "chunk_size", "bucket_plan", "model_state_bytes", "ring_traffic", "reduce_scatter",
+           "adamw_shard_step", "all_gather", "AdamW", "Scaler", "State", "Plan", "F16", "BF16", "F32"]

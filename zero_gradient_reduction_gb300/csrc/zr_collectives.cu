@@ -1,0 +1,327 @@
+// Standalone (unfused) kernels of the post-backward step: ring reduce-scatter,
+// the owner-side AdamW shard update (flag pass + conditional update), and the
+// parameter all-gather. Each is one HBM stream over its arrays; they are the
+// building blocks the fused step is measured against.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "zr_device.cuh"
+#include "zr_internal.h"
+
+using zr::fail;
+
+namespace {
+
+constexpr int kThreads = 256;
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+  }
+  return n;
+}
+
+int grid_for(int64_t work_items, int per_sm = 8) {
+  int64_t want = (work_items + kThreads - 1) / kThreads;
+  int64_t cap = (int64_t)sm_count() * per_sm;
+  if (want < 1) want = 1;
+  return (int)(want < cap ? want : cap);
+}
+
+zr_status launch_status(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(ZR_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  return ZR_OK;
+}
+
+// Block-wide OR of a per-thread flag, then one atomicOr per block.
+__device__ __forceinline__ void block_flag_or(bool mine, int32_t* flag_out) {
+  __shared__ int s_any;
+  if (threadIdx.x == 0) s_any = 0;
+  __syncthreads();
+  if (__any_sync(0xFFFFFFFFu, mine) && (threadIdx.x & 31) == 0) s_any = 1;
+  __syncthreads();
+  if (threadIdx.x == 0 && s_any) atomicOr(flag_out, 1);
+}
+
+// ---------------------------------------------------------------- reduce-scatter
+struct RsArgs {
+  const uint16_t* grads[ZR_MAX_W];  // indexed by worker
+  int order[ZR_MAX_W];              // ring position -> worker
+  float* sums;
+  int32_t* overflow;
+  int64_t n, C;
+  int W;
+};
+
+// Ring-order fp32 sum of the W values of element group e (8 elements, or the
+// ragged tail). Block c of the bucket starts at position c.
+template <int DT, int WT>
+__global__ void __launch_bounds__(kThreads) rs_kernel(const __grid_constant__ RsArgs a) {
+  const int W = WT > 0 ? WT : a.W;
+  bool bad = false;
+  const int64_t ngroups = (a.n + 7) / 8;
+  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < ngroups;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = g * 8;
+    const int c = (int)(e / a.C);
+    if (e + 8 <= a.n) {
+      float s[8];
+      if (WT > 0) {
+        uint4 raw[WT > 0 ? WT : 1];
+#pragma unroll
+        for (int h = 0; h < (WT > 0 ? WT : 1); ++h) {
+          int pos = c + h;
+          pos -= pos >= W ? W : 0;
+          raw[h] = zr::ld_once(a.grads[a.order[pos]] + e);
+        }
+        zr::unpack8<DT>(raw[0], s);
+#pragma unroll
+        for (int h = 1; h < (WT > 0 ? WT : 1); ++h) {
+          float x[8];
+          zr::unpack8<DT>(raw[h], x);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x[j]);
+        }
+      } else {
+        zr::unpack8<DT>(zr::ld_once(a.grads[a.order[c]] + e), s);
+        for (int h = 1; h < W; ++h) {
+          int pos = c + h;
+          pos -= pos >= W ? W : 0;
+          float x[8];
+          zr::unpack8<DT>(zr::ld_once(a.grads[a.order[pos]] + e), x);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x[j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bad |= zr::nonfinite(s[j]);
+      zr::st_once_f4(a.sums + e, make_float4(s[0], s[1], s[2], s[3]));
+      zr::st_once_f4(a.sums + e + 4, make_float4(s[4], s[5], s[6], s[7]));
+    } else {
+      for (int64_t i = e; i < a.n; ++i) {
+        float s = zr::to_f32<DT>(a.grads[a.order[c]][i]);
+        for (int h = 1; h < W; ++h) {
+          int pos = c + h;
+          pos -= pos >= W ? W : 0;
+          s = __fadd_rn(s, zr::to_f32<DT>(a.grads[a.order[pos]][i]));
+        }
+        bad |= zr::nonfinite(s);
+        a.sums[i] = s;
+      }
+    }
+  }
+  block_flag_or(bad, a.overflow);
+}
+
+template <int DT>
+void launch_rs(const RsArgs& a, int grid, cudaStream_t s) {
+  switch (a.W) {
+    case 1: rs_kernel<DT, 1><<<grid, kThreads, 0, s>>>(a); break;
+    case 2: rs_kernel<DT, 2><<<grid, kThreads, 0, s>>>(a); break;
+    case 3: rs_kernel<DT, 3><<<grid, kThreads, 0, s>>>(a); break;
+    case 4: rs_kernel<DT, 4><<<grid, kThreads, 0, s>>>(a); break;
+    case 8: rs_kernel<DT, 8><<<grid, kThreads, 0, s>>>(a); break;
+    default: rs_kernel<DT, 0><<<grid, kThreads, 0, s>>>(a); break;
+  }
+}
+
+// ---------------------------------------------------------------- AdamW shard step
+__global__ void __launch_bounds__(kThreads) flag_pass_kernel(const float* __restrict__ x, int64_t n,
+                                                              int32_t* overflow) {
+  bool bad = false;
+  const int64_t nv = n / 4;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nv; i += (int64_t)gridDim.x * blockDim.x) {
+    float4 v = zr::ld_once_f4(x + 4 * i);
+    bad |= zr::nonfinite(v.x) | zr::nonfinite(v.y) | zr::nonfinite(v.z) | zr::nonfinite(v.w);
+  }
+  for (int64_t i = nv * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    bad |= zr::nonfinite(x[i]);
+  block_flag_or(bad, overflow);
+}
+
+struct AdamArgs {
+  const float* sums;
+  float* m;
+  float* v;
+  float* master;
+  const int32_t* overflow;
+  int64_t n;
+  float r;  // fp32(1/(S*W))
+  zr::AdamConsts k;
+};
+
+__global__ void __launch_bounds__(kThreads) adamw_kernel(const __grid_constant__ AdamArgs a) {
+  __shared__ int s_skip;
+  if (threadIdx.x == 0) s_skip = *reinterpret_cast<const volatile int32_t*>(a.overflow);
+  __syncthreads();
+  if (s_skip) return;
+  const int64_t nv = a.n / 4;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nv; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = 4 * i;
+    float4 s = zr::ld_once_f4(a.sums + e), p = zr::ld_once_f4(a.master + e), m = zr::ld_once_f4(a.m + e),
+           v = zr::ld_once_f4(a.v + e);
+    zr::adamw_elem(__fmul_rn(s.x, a.r), p.x, m.x, v.x, a.k);
+    zr::adamw_elem(__fmul_rn(s.y, a.r), p.y, m.y, v.y, a.k);
+    zr::adamw_elem(__fmul_rn(s.z, a.r), p.z, m.z, v.z, a.k);
+    zr::adamw_elem(__fmul_rn(s.w, a.r), p.w, m.w, v.w, a.k);
+    zr::st_once_f4(a.master + e, p);
+    zr::st_once_f4(a.m + e, m);
+    zr::st_once_f4(a.v + e, v);
+  }
+  for (int64_t i = nv * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < a.n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float p = a.master[i], m = a.m[i], v = a.v[i];
+    zr::adamw_elem(__fmul_rn(a.sums[i], a.r), p, m, v, a.k);
+    a.master[i] = p;
+    a.m[i] = m;
+    a.v[i] = v;
+  }
+}
+
+// ---------------------------------------------------------------- all-gather
+struct AgArgs {
+  void* out[ZR_MAX_REPLICAS];
+  const float* master;
+  int64_t n;
+  int R;
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) ag_kernel(const __grid_constant__ AgArgs a) {
+  const int64_t ngroups = (a.n + 7) / 8;
+  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < ngroups;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = g * 8;
+    if (e + 8 <= a.n) {
+      float4 lo = zr::ld_once_f4(a.master + e), hi = zr::ld_once_f4(a.master + e + 4);
+      const float f[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+      const uint4 packed = zr::pack8<DT>(f);
+      for (int r = 0; r < a.R; ++r) zr::st_once(static_cast<uint16_t*>(a.out[r]) + e, packed);
+    } else {
+      for (int64_t i = e; i < a.n; ++i) {
+        const uint16_t b = zr::from_f32<DT>(a.master[i]);
+        for (int r = 0; r < a.R; ++r) static_cast<uint16_t*>(a.out[r])[i] = b;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+namespace zr {
+// fp32(1 - beta^t) with beta^t a running product of t double multiplications.
+float bias_correction_host(float beta, int64_t t) {
+  double prod = 1.0;
+  for (int64_t i = 0; i < t; ++i) prod = prod * (double)beta;
+  return (float)(1.0 - prod);
+}
+
+AdamConsts adam_consts_host(const zr_adamw_hyper& h, float bc1, float bc2) {
+  AdamConsts k;
+  k.b1 = h.beta1;
+  k.b2 = h.beta2;
+  k.omb1 = 1.0f - h.beta1;
+  k.omb2 = 1.0f - h.beta2;
+  k.lr = h.lr;
+  k.eps = h.eps;
+  const float lrwd = h.lr * h.weight_decay;
+  k.decay = 1.0f - lrwd;
+  k.bc1 = bc1;
+  k.bc2 = bc2;
+  return k;
+}
+}  // namespace zr
+
+extern "C" zr_status zr_reduce_scatter(const void* const* grads, zr_dtype dt, int64_t n, int W, const int* order,
+                                       float* sums, int32_t* overflow, void* stream) {
+  zr::clear_error();
+  if (n < 0) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: n < 0");
+  if (W < 1 || W > ZR_MAX_W) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: W=%d outside [1, %d]", W, ZR_MAX_W);
+  if (dt != ZR_F16 && dt != ZR_BF16) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: dtype must be F16 or BF16");
+  if (!grads || !sums || !overflow) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: null pointer");
+  if (!zr::aligned16(sums) || (reinterpret_cast<uintptr_t>(overflow) & 3u))
+    return fail(ZR_ERR_INVALID, "zr_reduce_scatter: misaligned output");
+  RsArgs a{};
+  bool seen[ZR_MAX_W] = {};
+  for (int p = 0; p < W; ++p) {
+    const int w = order ? order[p] : p;
+    if (w < 0 || w >= W || seen[w]) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: order is not a permutation");
+    seen[w] = true;
+    a.order[p] = w;
+  }
+  for (int w = 0; w < W; ++w) {
+    if (!grads[w] || !zr::aligned16(grads[w])) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: grads[%d] null or misaligned", w);
+    a.grads[w] = static_cast<const uint16_t*>(grads[w]);
+  }
+  if (n == 0) return ZR_OK;
+  a.sums = sums;
+  a.overflow = overflow;
+  a.n = n;
+  a.C = zr_chunk_size(n, W, ZR_ALIGN);
+  a.W = W;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int grid = grid_for((n + 7) / 8);
+  if (dt == ZR_F16) launch_rs<zr::DT_F16>(a, grid, s);
+  else launch_rs<zr::DT_BF16>(a, grid, s);
+  return launch_status("zr_reduce_scatter");
+}
+
+extern "C" zr_status zr_adamw_shard_step(const float* shard_sums, float* m, float* v, float* master, int64_t len,
+                                         const zr_adamw_hyper* h, float loss_scale, int W, int64_t t,
+                                         int32_t* overflow, void* stream) {
+  zr::clear_error();
+  if (len < 0) return fail(ZR_ERR_INVALID, "zr_adamw_shard_step: len < 0");
+  if (!h) return fail(ZR_ERR_INVALID, "zr_adamw_shard_step: null hyperparameters");
+  if (t < 1) return fail(ZR_ERR_INVALID, "zr_adamw_shard_step: t must be >= 1");
+  if (W < 1) return fail(ZR_ERR_INVALID, "zr_adamw_shard_step: W < 1");
+  if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale))
+    return fail(ZR_ERR_INVALID, "zr_adamw_shard_step: loss_scale must be positive and finite");
+  if (!shard_sums || !m || !v || !master || !overflow) return fail(ZR_ERR_INVALID, "zr_adamw_shard_step: null pointer");
+  if (!zr::aligned16(shard_sums) || !zr::aligned16(m) || !zr::aligned16(v) || !zr::aligned16(master))
+    return fail(ZR_ERR_INVALID, "zr_adamw_shard_step: misaligned array");
+  if (len == 0) return ZR_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  flag_pass_kernel<<<grid_for(len / 4 + 1), kThreads, 0, s>>>(shard_sums, len, overflow);
+  zr_status st = launch_status("zr_adamw_shard_step flag pass");
+  if (st != ZR_OK) return st;
+  AdamArgs a{};
+  a.sums = shard_sums;
+  a.m = m;
+  a.v = v;
+  a.master = master;
+  a.overflow = overflow;
+  a.n = len;
+  a.r = (float)(1.0 / ((double)loss_scale * (double)W));
+  a.k = zr::adam_consts_host(*h, zr::bias_correction_host(h->beta1, t), zr::bias_correction_host(h->beta2, t));
+  adamw_kernel<<<grid_for(len / 4 + 1), kThreads, 0, s>>>(a);
+  return launch_status("zr_adamw_shard_step update");
+}
+
+extern "C" zr_status zr_all_gather(const float* master, int64_t n, zr_dtype out_dt, void* const* replicas,
+                                   int n_replicas, void* stream) {
+  zr::clear_error();
+  if (n < 0) return fail(ZR_ERR_INVALID, "zr_all_gather: n < 0");
+  if (out_dt != ZR_F16 && out_dt != ZR_BF16) return fail(ZR_ERR_INVALID, "zr_all_gather: dtype must be F16 or BF16");
+  if (n_replicas < 1 || n_replicas > ZR_MAX_REPLICAS)
+    return fail(ZR_ERR_INVALID, "zr_all_gather: n_replicas=%d outside [1, %d]", n_replicas, ZR_MAX_REPLICAS);
+  if (!master || !replicas || !zr::aligned16(master)) return fail(ZR_ERR_INVALID, "zr_all_gather: null or misaligned master");
+  AgArgs a{};
+  for (int r = 0; r < n_replicas; ++r) {
+    if (!replicas[r] || !zr::aligned16(replicas[r])) return fail(ZR_ERR_INVALID, "zr_all_gather: replica %d null or misaligned", r);
+    a.out[r] = replicas[r];
+  }
+  if (n == 0) return ZR_OK;
+  a.master = master;
+  a.n = n;
+  a.R = n_replicas;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int grid = grid_for((n + 7) / 8);
+  if (out_dt == ZR_F16) ag_kernel<zr::DT_F16><<<grid, kThreads, 0, s>>>(a);
+  else ag_kernel<zr::DT_BF16><<<grid, kThreads, 0, s>>>(a);
+  return launch_status("zr_all_gather");
+}

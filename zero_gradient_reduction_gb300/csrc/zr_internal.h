@@ -1,0 +1,33 @@
+// Internal declarations shared by the libzr translation units (host side).
+#pragma once
+#include <cstdint>
+#include <string>
+
+#include "zr.h"
+
+namespace zr {
+
+// Thread-local last-error message; returns `s` for tail calls.
+zr_status fail(zr_status s, const char* fmt, ...);
+void clear_error();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Control block of a plan, resident in device memory. Written by the last block of
+// each fused step; read at the start of every block of the next one.
+struct Ctrl {
+  int32_t k;              // live state set
+  int32_t overflow;       // OR of this step's block flags (0 between steps)
+  uint32_t ticket;        // blocks finished in this step (0 between steps)
+  int32_t last_overflow;  // flag of the last finished step
+  float scale;            // loss scale for the next step
+  float scale_used;       // loss scale of the last finished step
+  int32_t dynamic;
+  int32_t interval;
+  float backoff, growth, min_scale;
+  int32_t stage;          // stage of the last step
+  int64_t good, t, steps, skipped;
+  double prod1, prod2;    // beta1^t, beta2^t (running products)
+};
+
+}  // namespace zr
