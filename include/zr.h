@@ -229,6 +229,47 @@ zr_status zr_step_from_host(zr_plan* p, int stage, const void* const* host_grads
 zr_status zr_plan_report(zr_plan* p, void* stream, zr_step_report* rep);
 
 /* ------------------------------------------------------------------------- */
+/* Fused step without device allocation                                        */
+/* ------------------------------------------------------------------------- */
+
+/* Tile capacity of the static scratch used by zr_step_noalloc: 16 bytes per tile of at
+ * most 8192 elements, i.e. 1 MiB of device memory per GPU, enough for about 5e8
+ * elements when the ring blocks are long. */
+#define ZR_NOALLOC_MAX_TILES 65536
+
+/* The pages have no counterpart to this call; it exists for callers that cannot
+ * allocate device memory. zr_plan_create allocates a tile table and a control block,
+ * which a caller cannot accept if its runtime owns all device memory through its own
+ * pool, if its memory budget was fixed before the first step, or if an allocation
+ * would synchronise the device on its path. zr_step_noalloc computes exactly what
+ * zr_step computes for one step, allocating nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine): its scratch is one static device array of this library
+ * (ZR_NOALLOC_MAX_TILES tiles plus a 256-byte header), present on every GPU that loads
+ * the library until the process exits.
+ *
+ * buckets[nbuckets]: host bucket table, e.g. from zr_bucket_plan (starts and lengths
+ * multiples of ZR_ALIGN, chunk = zr_chunk_size(len, W, ZR_ALIGN)). grads[W*A]: host
+ * array of device pointers, replica w*A + a, each covering every bucket. order: ring
+ * order (NULL = identity). st/current: reads state set `current`, writes set
+ * 1-current in full. loss_scale and t (1-based index of this update) as in
+ * zr_adamw_shard_step. overflow: device int32, set to 1 if any reduced gradient is
+ * not finite, else 0; when it is 1 the written set must be discarded (keep
+ * `current`), and the caller applies its own loss-scale rule.
+ * The caller carries the live-set index, the scale and t between calls.
+ *
+ * Every call on a device reuses the same scratch and leaves its last contents there;
+ * the call rebuilds the tile schedule and clears the ticket and flag itself. Calls
+ * whose kernels overlap on the GPU race on the scratch: order them on one stream (or
+ * otherwise serialise them). The first call on a device looks up the scratch's device
+ * address (cudaGetSymbolAddress); make it before any stream capture.
+ * Errors: ZR_ERR_INVALID for the cases of zr_step, a bucket that breaks the ring rule,
+ * current not 0/1, t < 1, a bad loss_scale, or buckets needing more than
+ * ZR_NOALLOC_MAX_TILES tiles (use zr_plan_create/zr_step for those); ZR_ERR_CUDA. */
+zr_status zr_step_noalloc(const zr_bucket* buckets, int nbuckets, int W, int A, zr_dtype dtype, const int* order,
+                          const void* const* grads, const zr_state* st, int current, const zr_adamw_hyper* h,
+                          float loss_scale, int64_t t, int32_t* overflow, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* Accounting                                                                 */
 /* ------------------------------------------------------------------------- */
 

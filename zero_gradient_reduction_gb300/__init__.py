@@ -327,5 +327,27 @@ class Plan:
             pass
 
 
+def step_noalloc(buckets: np.ndarray, W: int, A: int, dtype: int, grads: Sequence, state: State, current: int,
+                 hyper: AdamW, loss_scale: float, t: int, overflow, order: Optional[Sequence[int]] = None,
+                 stream=None) -> None:
+    """zr_step_noalloc: the fused step for callers that cannot allocate device memory (scratch lives in a
+    static device array of the library; the caller carries the live set, the scale and t)."""
+    fn = lib().zr_step_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.POINTER(StateC), ctypes.c_int, ctypes.POINTER(Hyper), ctypes.c_float,
+                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    b = np.asarray(buckets, dtype=np.int64).reshape(-1, 3)
+    table = (Bucket * max(len(b), 1))(*[Bucket(int(s), int(n), int(c)) for s, n, c in b])
+    ordc = (ctypes.c_int * W)(*order) if order is not None else None
+    arr = _ptr_array(grads)
+    st = state.c()
+    h = hyper.c()
+    _check(fn(ctypes.addressof(table), len(b), int(W), int(A), int(dtype),
+              ctypes.addressof(ordc) if ordc is not None else None, ctypes.addressof(arr), ctypes.byref(st),
+              int(current), ctypes.byref(h), float(loss_scale), int(t), _ptr(overflow), _stream_handle(stream)))
+
+
 __all__ = ["lib", "ZrError", "chunk_size", "bucket_plan", "model_state_bytes", "ring_traffic", "reduce_scatter",
-           "adamw_shard_step", "all_gather", "AdamW", "Scaler", "State", "Plan", "F16", "BF16", "F32"]
+           "adamw_shard_step", "all_gather", "AdamW", "Scaler", "State", "Plan", "step_noalloc", "F16", "BF16",
+           "F32"]
