@@ -28,7 +28,7 @@ float bias_correction_host(float beta, int64_t t);
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTileElems = 8192;  // elements per tile (a multiple of 8 * kThreads)
+constexpr int kTileElems = 16384;  // elements per tile (a multiple of 8 * kThreads)
 
 struct FusedArgs {
   const uint16_t* grads[ZR_MAX_REPLICAS];  // replica w*A + a
@@ -101,37 +101,38 @@ __device__ void finish_step(const FusedArgs& a) {
   __threadfence();
 }
 
-// Sum of worker `pos`'s A micro-batch values (fp32, micro-batch order).
-template <int DT, int AT>
-__device__ __forceinline__ void worker_sum(const uint16_t* const* ptrs, int A, int64_t off, float out[8]) {
-  const int nA = AT > 0 ? AT : A;
-  if (AT > 0) {
-    uint4 raw[AT > 0 ? AT : 1];
+// AdamW on one 8-element group whose ring sums are s[0..7], reading state set `cur`
+// at flat element e and writing set 1-cur; returns whether any sum was not finite.
+template <int DT>
+__device__ __forceinline__ bool update_group(const FusedArgs& a, const StepConsts& K, int64_t e, const float s[8],
+                                             float4 p0, float4 p1, float4 m0, float4 m1, float4 v0, float4 v1) {
+  float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+  float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  bool bad = false;
 #pragma unroll
-    for (int q = 0; q < (AT > 0 ? AT : 1); ++q) raw[q] = zr::ld_once(ptrs[q] + off);
-    zr::unpack8<DT>(raw[0], out);
-#pragma unroll
-    for (int q = 1; q < (AT > 0 ? AT : 1); ++q) {
-      float x[8];
-      zr::unpack8<DT>(raw[q], x);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) out[j] = __fadd_rn(out[j], x[j]);
-    }
-  } else {
-    zr::unpack8<DT>(zr::ld_once(ptrs[0] + off), out);
-    for (int q = 1; q < nA; ++q) {
-      float x[8];
-      zr::unpack8<DT>(zr::ld_once(ptrs[q] + off), x);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) out[j] = __fadd_rn(out[j], x[j]);
-    }
+  for (int j = 0; j < 8; ++j) {
+    bad |= zr::nonfinite(s[j]);
+    zr::adamw_elem(__fmul_rn(s[j], K.r), p[j], m[j], v[j], K.k);
   }
+  const int out = 1 - K.cur;
+  zr::st_once_f4(a.master[out] + e, make_float4(p[0], p[1], p[2], p[3]));
+  zr::st_once_f4(a.master[out] + e + 4, make_float4(p[4], p[5], p[6], p[7]));
+  zr::st_once_f4(a.m[out] + e, make_float4(m[0], m[1], m[2], m[3]));
+  zr::st_once_f4(a.m[out] + e + 4, make_float4(m[4], m[5], m[6], m[7]));
+  zr::st_once_f4(a.v[out] + e, make_float4(v[0], v[1], v[2], v[3]));
+  zr::st_once_f4(a.v[out] + e + 4, make_float4(v[4], v[5], v[6], v[7]));
+  zr::st_once(a.param[out] + e, zr::pack8<DT>(p));
+  return bad;
 }
 
+// Ring-position pointers are computed per tile from the grid constants (block index c
+// is uniform over the tile), so tiles need no shared table and no block barrier. For
+// A = 1 with a compile-time W all W gradient loads and the six state loads of a group
+// are issued before any arithmetic.
 template <int DT, int WT, int AT>
-__global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_constant__ FusedArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_constant__ FusedArgs a) {
   __shared__ StepConsts s_k;
-  __shared__ const uint16_t* s_ptr[ZR_MAX_REPLICAS];  // tile's replica pointers in ring order
   __shared__ int s_bad;
   __shared__ unsigned s_ticket;
   if (threadIdx.x == 0) {
@@ -145,65 +146,84 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const __grid_const
   const float* __restrict__ mst_in = a.master[K.cur];
   const float* __restrict__ m_in = a.m[K.cur];
   const float* __restrict__ v_in = a.v[K.cur];
-  float* __restrict__ mst_out = a.master[1 - K.cur];
-  float* __restrict__ m_out = a.m[1 - K.cur];
-  float* __restrict__ v_out = a.v[1 - K.cur];
-  uint16_t* __restrict__ prm_out = a.param[1 - K.cur];
   bool bad = false;
 
   for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
     const int4 d = a.tiles[tile];
     const int64_t start = (int64_t)(((uint64_t)(uint32_t)d.y << 32) | (uint32_t)d.x);
     const int groups = d.z, c = d.w;
-    __syncthreads();  // previous tile's pointers are no longer in use
-    for (int i = threadIdx.x; i < W * A; i += blockDim.x) {
-      const int h = i / A, q = i - h * A;
-      int pos = c + h;
-      pos -= pos >= W ? W : 0;
-      s_ptr[i] = a.grads[a.order[pos] * A + q] + start;
-    }
-    __syncthreads();
-    for (int g = threadIdx.x; g < groups; g += blockDim.x) {
-      const int64_t off = (int64_t)g * 8;
-      float s[8];
-      if (WT > 0) {
-        float wsum[WT > 0 ? WT : 1][8];
+    if (WT > 0 && AT == 1) {
+      constexpr int WN = WT > 0 ? WT : 1;
+      const uint16_t* gp[WN];
 #pragma unroll
-        for (int h = 0; h < (WT > 0 ? WT : 1); ++h) worker_sum<DT, AT>(s_ptr + h * A, A, off, wsum[h]);
+      for (int h = 0; h < WN; ++h) {
+        int pos = c + h;
+        pos -= pos >= WN ? WN : 0;
+        gp[h] = a.grads[a.order[pos]] + start;
+      }
+      // U groups per thread and iteration, all of their loads issued before any arithmetic:
+      // with few replicas one group holds too few bytes in flight to cover HBM latency.
+      constexpr int UN = WN <= 3 ? 2 : 1;
+      for (int g0 = threadIdx.x; g0 < groups; g0 += UN * blockDim.x) {
+        uint4 raw[UN][WN];
+        float4 st[UN][6];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) s[j] = wsum[0][j];
+        for (int u = 0; u < UN; ++u) {
+          const int g = g0 + u * (int)blockDim.x;
+          if (g < groups) {
+            const int64_t off = (int64_t)g * 8, e = start + off;
 #pragma unroll
-        for (int h = 1; h < (WT > 0 ? WT : 1); ++h)
+            for (int h = 0; h < WN; ++h) raw[u][h] = zr::ld_once(gp[h] + off);
+            st[u][0] = zr::ld_once_f4(mst_in + e);
+            st[u][1] = zr::ld_once_f4(mst_in + e + 4);
+            st[u][2] = zr::ld_once_f4(m_in + e);
+            st[u][3] = zr::ld_once_f4(m_in + e + 4);
+            st[u][4] = zr::ld_once_f4(v_in + e);
+            st[u][5] = zr::ld_once_f4(v_in + e + 4);
+          }
+        }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], wsum[h][j]);
-      } else {
-        worker_sum<DT, AT>(s_ptr, A, off, s);
-        for (int h = 1; h < W; ++h) {
-          float x[8];
-          worker_sum<DT, AT>(s_ptr + h * A, A, off, x);
+        for (int u = 0; u < UN; ++u) {
+          const int g = g0 + u * (int)blockDim.x;
+          if (g < groups) {
+            float s[8];
+            zr::unpack8<DT>(raw[u][0], s);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x[j]);
+            for (int h = 1; h < WN; ++h) {
+              float x[8];
+              zr::unpack8<DT>(raw[u][h], x);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x[j]);
+            }
+            bad |= update_group<DT>(a, K, start + (int64_t)g * 8, s, st[u][0], st[u][1], st[u][2], st[u][3],
+                                    st[u][4], st[u][5]);
+          }
         }
       }
-      const int64_t e = start + off;
-      const float4 p0 = zr::ld_once_f4(mst_in + e), p1 = zr::ld_once_f4(mst_in + e + 4);
-      const float4 m0 = zr::ld_once_f4(m_in + e), m1 = zr::ld_once_f4(m_in + e + 4);
-      const float4 v0 = zr::ld_once_f4(v_in + e), v1 = zr::ld_once_f4(v_in + e + 4);
-      float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-      float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-      float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    } else {
+      for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+        const int64_t off = (int64_t)g * 8, e = start + off;
+        float s[8];
+        for (int h = 0; h < W; ++h) {
+          int pos = c + h;
+          pos -= pos >= W ? W : 0;
+          const uint16_t* const* rep = a.grads + a.order[pos] * A;  // worker's A micro-batches
+          float w8[8];
+          zr::unpack8<DT>(zr::ld_once(rep[0] + e), w8);
+          for (int q = 1; q < A; ++q) {
+            float x[8];
+            zr::unpack8<DT>(zr::ld_once(rep[q] + e), x);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        bad |= zr::nonfinite(s[j]);
-        zr::adamw_elem(__fmul_rn(s[j], K.r), p[j], m[j], v[j], K.k);
+            for (int j = 0; j < 8; ++j) w8[j] = __fadd_rn(w8[j], x[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) s[j] = h == 0 ? w8[j] : __fadd_rn(s[j], w8[j]);
+        }
+        const float4 p0 = zr::ld_once_f4(mst_in + e), p1 = zr::ld_once_f4(mst_in + e + 4);
+        const float4 m0 = zr::ld_once_f4(m_in + e), m1 = zr::ld_once_f4(m_in + e + 4);
+        const float4 v0 = zr::ld_once_f4(v_in + e), v1 = zr::ld_once_f4(v_in + e + 4);
+        bad |= update_group<DT>(a, K, e, s, p0, p1, m0, m1, v0, v1);
       }
-      zr::st_once_f4(mst_out + e, make_float4(p[0], p[1], p[2], p[3]));
-      zr::st_once_f4(mst_out + e + 4, make_float4(p[4], p[5], p[6], p[7]));
-      zr::st_once_f4(m_out + e, make_float4(m[0], m[1], m[2], m[3]));
-      zr::st_once_f4(m_out + e + 4, make_float4(m[4], m[5], m[6], m[7]));
-      zr::st_once_f4(v_out + e, make_float4(v[0], v[1], v[2], v[3]));
-      zr::st_once_f4(v_out + e + 4, make_float4(v[4], v[5], v[6], v[7]));
-      zr::st_once(prm_out + e, zr::pack8<DT>(p));
     }
   }
 
