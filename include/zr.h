@@ -218,10 +218,13 @@ zr_status zr_plan_reset(zr_plan* p, void* stream);
 zr_status zr_step(zr_plan* p, int stage, const void* const* grads, const zr_state* st,
                   const zr_adamw_hyper* h, void* stream, zr_step_report* rep);
 
-/* As zr_step, with the gradients in HOST memory: copies host_grads[r] (pinned host
- * memory gives full speed) into the device buffers dev_grads[r] with one
- * cudaMemcpyAsync per replica and bucket, launches the step, and reads the report
- * back (rep is required). Bucket b's copies are issued in bucket order. */
+/* As zr_step, with the gradients in HOST memory, and the report read back (rep is
+ * required). If every host_grads[r] is page-locked memory the device can address
+ * (cudaHostAlloc, cudaHostRegister; torch's pin_memory), the step kernel reads it in
+ * place over the host link, so each gradient byte crosses the link once while the HBM
+ * half of the step overlaps the transfer; dev_grads is then not used (may hold NULLs).
+ * Otherwise each host_grads[r] is copied into the device buffer dev_grads[r] with one
+ * cudaMemcpyAsync per replica and bucket, in bucket order, before the step. */
 zr_status zr_step_from_host(zr_plan* p, int stage, const void* const* host_grads, void* const* dev_grads,
                             const zr_state* st, const zr_adamw_hyper* h, void* stream, zr_step_report* rep);
 

@@ -333,7 +333,9 @@ def test_stages_identical():
     assert outs[0] == outs[1] == outs[2]
 
 
-def test_step_from_host_equals_step():
+@pytest.mark.parametrize("pinned", [True, False])
+def test_step_from_host_equals_step(pinned):
+    """Pinned host gradients are read in place by the kernel; pageable ones are copied first."""
     numels = [50_000, 777, 12_345]
     a = FusedRun(numels, 3, 1, zr.F16, cap=40_000, S=1024.0, seed=2)
     b = FusedRun(numels, 3, 1, zr.F16, cap=40_000, S=1024.0, seed=2)
@@ -341,13 +343,17 @@ def test_step_from_host_equals_step():
         a.step(s)
         host = []
         for r in range(3):
-            h = torch.from_numpy(b.layout.grads_host(0, b.n, s, r, b.S).view(np.int16).copy()).pin_memory()
-            host.append(h)
+            g = b.layout.grads_host(0, b.n, s, r, b.S)
+            host.append(torch.from_numpy(g.view(np.int16).copy()).pin_memory() if pinned else g.copy())
+        for d in b.grads:
+            d.fill_(0)
         rep = b.plan.step_from_host(host, b.grads, b.state, HYPER)
         assert rep.t == s and rep.overflow == 0
         b.current = rep.current
         for x, y in zip(a.live(), b.live()):
             assert x.tobytes() == y.tobytes()
+        # the copy path fills the device buffers; the in-place path leaves them alone
+        assert (int(b.grads[0].view(torch.int16).abs().sum().item()) == 0) == pinned
 
 
 def test_error_paths():

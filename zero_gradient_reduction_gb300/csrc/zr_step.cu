@@ -518,13 +518,36 @@ extern "C" zr_status zr_step_from_host(zr_plan* p, int stage, const void* const*
                                        const zr_state* st, const zr_adamw_hyper* h, void* stream,
                                        zr_step_report* rep) {
   zr::clear_error();
-  if (!host_grads || !dev_grads || !rep) return fail(ZR_ERR_INVALID, "zr_step_from_host: null argument");
-  zr_status s = check_step_args(p, stage, const_cast<const void* const*>(dev_grads), st, h);
-  if (s != ZR_OK) return s;
+  if (!p || !host_grads || !dev_grads || !rep) return fail(ZR_ERR_INVALID, "zr_step_from_host: null argument");
   const int R = p->W * p->A;
   for (int r = 0; r < R; ++r)
     if (!host_grads[r]) return fail(ZR_ERR_INVALID, "zr_step_from_host: host_grads[%d] is null", r);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // Page-locked host memory the device can address (cudaHostAlloc, cudaHostRegister) is read
+  // in place by the step kernel: each byte crosses the host link once and the HBM half of
+  // the step overlaps the transfer. Anything else is copied into dev_grads first.
+  bool direct = true;
+  const void* mapped[ZR_MAX_REPLICAS];
+  for (int r = 0; r < R && direct; ++r) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, host_grads[r]) != cudaSuccess) {
+      cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+      direct = false;
+    } else if (at.type != cudaMemoryTypeHost || !at.devicePointer) {
+      direct = false;
+    } else {
+      mapped[r] = at.devicePointer;
+    }
+  }
+  if (direct) {
+    zr_status s = check_step_args(p, stage, mapped, st, h);
+    if (s != ZR_OK) return s;
+    s = launch_step(p, stage, mapped, st, h, cs);
+    if (s != ZR_OK) return s;
+    return zr_plan_report(p, stream, rep);
+  }
+  zr_status s = check_step_args(p, stage, const_cast<const void* const*>(dev_grads), st, h);
+  if (s != ZR_OK) return s;
   for (const zr_bucket& b : p->buckets) {
     for (int r = 0; r < R; ++r) {
       const size_t off = (size_t)b.start * 2, bytes = (size_t)b.len * 2;
