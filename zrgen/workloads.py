@@ -96,6 +96,11 @@ WORKLOADS = {
                    sigma=1e-2, init_scale=65536.0, dynamic=True, inject_step=3,
                    description="flat 7.0e9 params in 200M-param buckets, W=2, fp16, dynamic loss scale S0=65536, "
                                "+inf injected at step 3"),
+    # the 7B workload's kernel configuration (W=2, fp16, 200M-param buckets) at 1/35 of its size: a case small
+    # enough for a full profiler capture
+    "7b_slice": Workload("7b_slice", _flat(200_000_000, 1), W=2, A=1, dtype=0, stage=1, cap=200_000_000, steps=6,
+                         seed=0, sigma=1e-2, init_scale=65536.0, dynamic=True,
+                         description="one 200M-param bucket of the 7B workload (W=2, fp16, S0=65536)"),
 }
 
 
