@@ -39,6 +39,22 @@ def _dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """The largest value of x over all ranks (x itself when running alone)."""
+    if ws <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, seconds_max: float, ws: int) -> float:
+    """Units processed by all ranks per second of the slowest rank, in billions."""
+    return ws * units_per_rank / seconds_max / 1e9
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -55,7 +71,7 @@ def _traffic_record(workload: str):
     import hashlib
     src = os.path.join(ROOT, "zero_gradient_reduction_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("zr_step.cu", "zr_device.cuh"):
+    for f in ("zr_step_kernel.cuh", "zr_device.cuh"):
         with open(os.path.join(src, f), "rb") as fh:
             h.update(fh.read())
     digest = h.hexdigest()[:16]
@@ -67,7 +83,7 @@ def _traffic_record(workload: str):
         for line in f:
             if line.startswith("- ") and ":" in line:
                 k, v = line[2:].split(":", 1)
-                rec[k.strip()] = v.strip().strip("`")
+                rec[k.strip()] = v.strip().split()[0].strip("`")
     if rec.get("kernel_source_sha256_16") != digest:
         return None, digest
     try:
@@ -289,13 +305,9 @@ def run_zr(args, w):
     rep = plan.report(stream)
     assert rep.overflow == 0 and rep.steps == args.warmup + args.steps * attempts, rep.as_dict()
 
-    ms_max = ms_total
-    if ws > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms_total, ws, dev)
     ms_step = ms_max / args.steps
-    value = ws * plan.n_real / (ms_step * 1e-3) / 1e9
+    value = whole_job_rate(plan.n_real, ms_step * 1e-3, ws)
 
     # roofline of the fused kernel: one launch per step, algorithmic bytes (2*W*A + 26) per param
     peak, peak_kind = _peaks()
@@ -316,12 +328,8 @@ def run_zr(args, w):
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
             r = plan.step_from_host(host, dgr, state, hyper, stream=stream)
-        dt = time.perf_counter() - t0
-        if ws > 1:
-            t = torch.tensor([dt], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": ws * plan.n_real * args.e2e_steps / dt / 1e9, "unit": "Gparams/s",
+        dt = max_over_ranks(time.perf_counter() - t0, ws, dev)
+        e2e = {"value": whole_job_rate(plan.n_real * args.e2e_steps, dt, ws), "unit": "Gparams/s",
                "h2d_bytes_per_step": int(2 * n * w.W * w.A), "d2h_bytes_per_step": int(__import__("ctypes").sizeof(r)),
                "ms_per_step": dt / args.e2e_steps * 1e3, "steps": args.e2e_steps,
                "api": "zr_step_from_host (pinned host grads -> device, fused step, report read back)"}

@@ -231,6 +231,25 @@ zr_status zr_step_from_host(zr_plan* p, int stage, const void* const* host_grads
 /* Synchronises `stream` and reads the control block into *rep. */
 zr_status zr_plan_report(zr_plan* p, void* stream, zr_step_report* rep);
 
+/* Checkpoint / resume of a plan's step state (the pages name checkpoints among the
+ * runtime's duties, [P2] 2 (1) ②, without a mechanism). The optimizer state and the
+ * replica live in caller buffers, which the caller saves itself (the live set is
+ * `current`); this record holds what the control block adds. Restoring it into a plan
+ * with the same layout and continuing gives the same bytes as never stopping. */
+typedef struct {
+    int32_t current;       /* live state set */
+    float scale;           /* loss scale for the next step */
+    int64_t good, t, steps, skipped;
+    double beta1_pow, beta2_pow; /* beta1^t, beta2^t as running products */
+} zr_checkpoint;
+
+/* Synchronises `stream` and copies the control block into *out. */
+zr_status zr_plan_checkpoint(zr_plan* p, void* stream, zr_checkpoint* out);
+/* Writes *in into the control block on `stream` and synchronises it.
+ * Errors: ZR_ERR_INVALID for a null argument, current not 0/1, a scale that is not
+ * positive and finite, negative counters. */
+zr_status zr_plan_restore(zr_plan* p, const zr_checkpoint* in, void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* Fused step without device allocation                                        */
 /* ------------------------------------------------------------------------- */

@@ -54,6 +54,12 @@ class StateC(ctypes.Structure):
                 ("param", ctypes.c_void_p * 2)]
 
 
+class Checkpoint(ctypes.Structure):
+    _fields_ = [("current", ctypes.c_int32), ("scale", ctypes.c_float), ("good", ctypes.c_int64),
+                ("t", ctypes.c_int64), ("steps", ctypes.c_int64), ("skipped", ctypes.c_int64),
+                ("beta1_pow", ctypes.c_double), ("beta2_pow", ctypes.c_double)]
+
+
 class StepReport(ctypes.Structure):
     _fields_ = [("overflow", ctypes.c_int32), ("skipped", ctypes.c_int32), ("current", ctypes.c_int32),
                 ("stage", ctypes.c_int32), ("scale_used", ctypes.c_float), ("scale", ctypes.c_float),
@@ -95,6 +101,8 @@ def lib():
                 "zr_step_from_host": (st, [vp, i32, vp, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp,
                                            ctypes.POINTER(StepReport)]),
                 "zr_plan_report": (st, [vp, vp, ctypes.POINTER(StepReport)]),
+                "zr_plan_checkpoint": (st, [vp, vp, ctypes.POINTER(Checkpoint)]),
+                "zr_plan_restore": (st, [vp, ctypes.POINTER(Checkpoint), vp]),
                 "zr_model_state_bytes": (i64, [i32, i64, i32]),
                 "zr_ring_traffic": (st, [i64, i32, i32, vp, vp, vp, vp]),
                 "zr_status_str": (ctypes.c_char_p, [st]),
@@ -311,6 +319,15 @@ class Plan:
         rep = StepReport()
         _check(lib().zr_plan_report(self._h, _stream_handle(stream), ctypes.byref(rep)))
         return rep
+
+    def checkpoint(self, stream=None) -> Checkpoint:
+        """The control block's step state (live set, scale, t, ...); save the live state tensors with it."""
+        c = Checkpoint()
+        _check(lib().zr_plan_checkpoint(self._h, _stream_handle(stream), ctypes.byref(c)))
+        return c
+
+    def restore(self, ckpt: Checkpoint, stream=None) -> None:
+        _check(lib().zr_plan_restore(self._h, ctypes.byref(ckpt), _stream_handle(stream)))
 
     def reset(self, stream=None) -> None:
         _check(lib().zr_plan_reset(self._h, _stream_handle(stream)))

@@ -21,7 +21,8 @@ ARCH = os.environ.get("ZR_CUDA_ARCH", "103a")
 
 CU = ["zr_step.cu", "zr_collectives.cu", "zr_noalloc.cu"]
 CPP = ["zr_host.cpp"]
-HEADERS = [os.path.join(INCLUDE, "zr.h"), os.path.join(CSRC, "zr_internal.h"), os.path.join(CSRC, "zr_device.cuh")]
+HEADERS = [os.path.join(INCLUDE, "zr.h"), os.path.join(CSRC, "zr_internal.h"), os.path.join(CSRC, "zr_device.cuh"),
+           os.path.join(CSRC, "zr_step_kernel.cuh")]
 
 
 def _nvcc_flags(verbose_ptxas: bool = False):

@@ -1,0 +1,255 @@
+// Device side of the fused post-backward step (included by zr_step.cu): the kernel
+// arguments, the per-step constants read from the control block, the last-block
+// epilogue and fused_step_kernel itself.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "zr_device.cuh"
+#include "zr_internal.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTileElems = 16384;  // elements per tile (a multiple of 8 * kThreads)
+
+struct FusedArgs {
+  const uint16_t* grads[ZR_MAX_REPLICAS];  // replica w*A + a
+  int order[ZR_MAX_W];                     // ring position -> worker
+  const int4* tiles;                       // {start lo, start hi, groups, block index c}
+  int64_t ntiles;
+  float* master[2];
+  float* m[2];
+  float* v[2];
+  uint16_t* param[2];
+  zr::Ctrl* ctrl;
+  float lr, beta1, beta2, eps, weight_decay;
+  int W, A, stage;
+};
+
+// Per-block view of the control block, read once at the start of the step.
+struct StepConsts {
+  zr::AdamConsts k;
+  float r;  // fp32(1/(S*W))
+  int cur;  // live state set
+};
+
+__device__ void read_consts(const FusedArgs& a, StepConsts& out) {
+  const volatile zr::Ctrl* c = a.ctrl;
+  const double S = (double)c->scale;
+  const double p1 = c->prod1, p2 = c->prod2;
+  out.cur = c->k;
+  out.r = (float)__ddiv_rn(1.0, __dmul_rn(S, (double)a.W));
+  out.k.b1 = a.beta1;
+  out.k.b2 = a.beta2;
+  out.k.omb1 = __fsub_rn(1.0f, a.beta1);
+  out.k.omb2 = __fsub_rn(1.0f, a.beta2);
+  out.k.lr = a.lr;
+  out.k.eps = a.eps;
+  out.k.decay = __fsub_rn(1.0f, __fmul_rn(a.lr, a.weight_decay));
+  out.k.bc1 = (float)__dsub_rn(1.0, __dmul_rn(p1, (double)a.beta1));
+  out.k.bc2 = (float)__dsub_rn(1.0, __dmul_rn(p2, (double)a.beta2));
+}
+
+// The loss-scale rule and commit, run by one thread of the last block.
+__device__ void finish_step(const FusedArgs& a) {
+  volatile zr::Ctrl* c = a.ctrl;
+  const int of = c->overflow;
+  float scale = c->scale;
+  c->last_overflow = of;
+  c->scale_used = scale;
+  c->stage = a.stage;
+  c->steps = c->steps + 1;
+  if (of) {
+    c->skipped = c->skipped + 1;
+    if (c->dynamic) {
+      const float s2 = __fmul_rn(scale, c->backoff);
+      scale = s2 > c->min_scale ? s2 : c->min_scale;
+      c->good = 0;
+    }
+  } else {
+    c->t = c->t + 1;
+    c->prod1 = __dmul_rn(c->prod1, (double)a.beta1);
+    c->prod2 = __dmul_rn(c->prod2, (double)a.beta2);
+    c->k = 1 - c->k;
+    c->good = c->good + 1;
+    if (c->dynamic && c->good >= c->interval) {
+      scale = __fmul_rn(scale, c->growth);
+      c->good = 0;
+    }
+  }
+  c->scale = scale;
+  c->overflow = 0;
+  c->ticket = 0;
+  __threadfence();
+}
+
+// AdamW on one 8-element group whose ring sums are s[0..7], reading state set `cur`
+// at flat element e and writing set 1-cur; returns whether any sum was not finite.
+template <int DT>
+__device__ __forceinline__ bool update_group(const FusedArgs& a, const StepConsts& K, int64_t e, const float s[8],
+                                             float4 p0, float4 p1, float4 m0, float4 m1, float4 v0, float4 v1) {
+  float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+  float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    bad |= zr::nonfinite(s[j]);
+    zr::adamw_elem(__fmul_rn(s[j], K.r), p[j], m[j], v[j], K.k);
+  }
+  const int out = 1 - K.cur;
+  zr::st_once_f4(a.master[out] + e, make_float4(p[0], p[1], p[2], p[3]));
+  zr::st_once_f4(a.master[out] + e + 4, make_float4(p[4], p[5], p[6], p[7]));
+  zr::st_once_f4(a.m[out] + e, make_float4(m[0], m[1], m[2], m[3]));
+  zr::st_once_f4(a.m[out] + e + 4, make_float4(m[4], m[5], m[6], m[7]));
+  zr::st_once_f4(a.v[out] + e, make_float4(v[0], v[1], v[2], v[3]));
+  zr::st_once_f4(a.v[out] + e + 4, make_float4(v[4], v[5], v[6], v[7]));
+  zr::st_once(a.param[out] + e, zr::pack8<DT>(p));
+  return bad;
+}
+
+// Ring-position pointers are computed per tile from the grid constants (block index c
+// is uniform over the tile), so tiles need no shared table and no block barrier. For
+// A = 1 with a compile-time W all W gradient loads and the six state loads of a group
+// are issued before any arithmetic.
+template <int DT, int WT, int AT>
+__global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_constant__ FusedArgs a) {
+  __shared__ StepConsts s_k;
+  __shared__ int s_bad;
+  __shared__ unsigned s_ticket;
+  if (threadIdx.x == 0) {
+    read_consts(a, s_k);
+    s_bad = 0;
+  }
+  __syncthreads();
+  const StepConsts K = s_k;
+  const int W = WT > 0 ? WT : a.W;
+  const int A = AT > 0 ? AT : a.A;
+  const float* __restrict__ mst_in = a.master[K.cur];
+  const float* __restrict__ m_in = a.m[K.cur];
+  const float* __restrict__ v_in = a.v[K.cur];
+  bool bad = false;
+
+  for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+    const int4 d = a.tiles[tile];
+    const int64_t start = (int64_t)(((uint64_t)(uint32_t)d.y << 32) | (uint32_t)d.x);
+    const int groups = d.z, c = d.w;
+    if (WT > 0 && AT == 1) {
+      constexpr int WN = WT > 0 ? WT : 1;
+      const uint16_t* gp[WN];
+#pragma unroll
+      for (int h = 0; h < WN; ++h) {
+        int pos = c + h;
+        pos -= pos >= WN ? WN : 0;
+        gp[h] = a.grads[a.order[pos]] + start;
+      }
+      // U groups per thread and iteration, all of their loads issued before any arithmetic:
+      // with few replicas one group holds too few bytes in flight to cover HBM latency.
+      constexpr int UN = WN <= 3 ? 2 : 1;
+      for (int g0 = threadIdx.x; g0 < groups; g0 += UN * blockDim.x) {
+        uint4 raw[UN][WN];
+        float4 st[UN][6];
+#pragma unroll
+        for (int u = 0; u < UN; ++u) {
+          const int g = g0 + u * (int)blockDim.x;
+          if (g < groups) {
+            const int64_t off = (int64_t)g * 8, e = start + off;
+#pragma unroll
+            for (int h = 0; h < WN; ++h) raw[u][h] = zr::ld_once(gp[h] + off);
+            st[u][0] = zr::ld_once_f4(mst_in + e);
+            st[u][1] = zr::ld_once_f4(mst_in + e + 4);
+            st[u][2] = zr::ld_once_f4(m_in + e);
+            st[u][3] = zr::ld_once_f4(m_in + e + 4);
+            st[u][4] = zr::ld_once_f4(v_in + e);
+            st[u][5] = zr::ld_once_f4(v_in + e + 4);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < UN; ++u) {
+          const int g = g0 + u * (int)blockDim.x;
+          if (g < groups) {
+            float s[8];
+            zr::unpack8<DT>(raw[u][0], s);
+#pragma unroll
+            for (int h = 1; h < WN; ++h) {
+              float x[8];
+              zr::unpack8<DT>(raw[u][h], x);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x[j]);
+            }
+            bad |= update_group<DT>(a, K, start + (int64_t)g * 8, s, st[u][0], st[u][1], st[u][2], st[u][3],
+                                    st[u][4], st[u][5]);
+          }
+        }
+      }
+    } else {
+      for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+        const int64_t off = (int64_t)g * 8, e = start + off;
+        float s[8];
+        for (int h = 0; h < W; ++h) {
+          int pos = c + h;
+          pos -= pos >= W ? W : 0;
+          const uint16_t* const* rep = a.grads + a.order[pos] * A;  // worker's A micro-batches
+          float w8[8];
+          zr::unpack8<DT>(zr::ld_once(rep[0] + e), w8);
+          for (int q = 1; q < A; ++q) {
+            float x[8];
+            zr::unpack8<DT>(zr::ld_once(rep[q] + e), x);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) w8[j] = __fadd_rn(w8[j], x[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) s[j] = h == 0 ? w8[j] : __fadd_rn(s[j], w8[j]);
+        }
+        const float4 p0 = zr::ld_once_f4(mst_in + e), p1 = zr::ld_once_f4(mst_in + e + 4);
+        const float4 m0 = zr::ld_once_f4(m_in + e), m1 = zr::ld_once_f4(m_in + e + 4);
+        const float4 v0 = zr::ld_once_f4(v_in + e), v1 = zr::ld_once_f4(v_in + e + 4);
+        bad |= update_group<DT>(a, K, e, s, p0, p1, m0, m1, v0, v1);
+      }
+    }
+  }
+
+  // Block flag -> control block, then the ticket: the last block to arrive decides.
+  if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0) s_bad = 1;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (s_bad) atomicOr(&a.ctrl->overflow, 1);
+    __threadfence();
+    s_ticket = atomicAdd(&a.ctrl->ticket, 1u);
+  }
+  __syncthreads();
+  if (s_ticket == gridDim.x - 1 && threadIdx.x == 0) {
+    __threadfence();
+    finish_step(a);
+  }
+}
+
+using KernelFn = void (*)(FusedArgs);
+
+template <int DT>
+KernelFn pick_kernel(int W, int A) {
+  if (A == 1) {
+    switch (W) {
+      case 1: return fused_step_kernel<DT, 1, 1>;
+      case 2: return fused_step_kernel<DT, 2, 1>;
+      case 3: return fused_step_kernel<DT, 3, 1>;
+      case 4: return fused_step_kernel<DT, 4, 1>;
+      case 8: return fused_step_kernel<DT, 8, 1>;
+      default: return fused_step_kernel<DT, 0, 1>;
+    }
+  }
+  if (A == 4) {
+    switch (W) {
+      case 2: return fused_step_kernel<DT, 2, 4>;
+      case 4: return fused_step_kernel<DT, 4, 4>;
+      case 8: return fused_step_kernel<DT, 8, 4>;
+      default: return fused_step_kernel<DT, 0, 4>;
+    }
+  }
+  return fused_step_kernel<DT, 0, 0>;
+}
+
+}  // namespace
+
