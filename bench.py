@@ -314,6 +314,40 @@ def run_zr(args, w):
     achieved = rep.bytes_alg / (ms_total / args.steps * 1e-3) / 1e9
     traffic, _digest = _traffic_record(w.name)
 
+    # comparison point: the same step as the unfused chain of standalone calls (reduce-scatter per bucket
+    # into fp32 sums, flag pass + AdamW in place, cast/all-gather), (2W + 38) bytes per param
+    chain = None
+    if w.A == 1 and not args.no_chain:
+        sums = torch.empty(n, dtype=torch.float32, device=dev)
+        flag = torch.zeros(1, dtype=torch.int32, device=dev)
+        k = rep.current
+
+        def chain_step():
+            for (b0, blen, _c) in plan.buckets:
+                views = [g[b0:b0 + blen] for g in grads]
+                zr.reduce_scatter(views, sums[b0:b0 + blen], flag, stream=stream)
+            zr.adamw_shard_step(sums, state.m[k], state.v[k], state.master[k], hyper, w.init_scale, w.W, 1, flag,
+                                stream=stream)
+            zr.all_gather(state.master[k], [state.param[k]], stream=stream)
+
+        for _ in range(3):
+            chain_step()
+        torch.cuda.synchronize(dev)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(args.chain_steps):
+            chain_step()
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        chain_ms = c0.elapsed_time(c1) / args.chain_steps
+        chain_bytes = (2 * w.W + 38) * plan.n_real
+        chain = {"ms_per_step": chain_ms, "Gparams_per_s": plan.n_real / chain_ms / 1e6,
+                 "alg_bytes_per_param": 2 * w.W + 38, "hbm_GBs": chain_bytes / chain_ms / 1e6,
+                 "launches_per_step": len(plan.buckets) + 3,
+                 "calls": "zr_reduce_scatter per bucket, zr_adamw_shard_step, zr_all_gather"}
+        del sums
+
     e2e = None
     cpu = None
     if not args.no_e2e:
@@ -353,6 +387,7 @@ def run_zr(args, w):
                      "kernel": "fused_step_kernel (one launch per step)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "unfused_chain": chain,
         "gpu_launches": args.steps,
         "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
                    "reasons": clocks.get("reasons"), "samples": clocks.get("samples"),
@@ -377,6 +412,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-chain", action="store_true")
+    ap.add_argument("--chain-steps", type=int, default=5)
     args = ap.parse_args()
     if args.warmup < 3:
         print(f"bench: raising --warmup {args.warmup} to the minimum of 3", file=sys.stderr)

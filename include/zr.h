@@ -103,8 +103,9 @@ zr_status zr_bucket_plan(const int64_t* numels, int ntensors, int64_t cap_elems,
 
 /* Ring reduce-scatter of one n-element bucket over W workers ([P1] 二 scatter reduce,
  * GPU0/GPU1/GPU2 example; [P3] Ring AllReduce 阶段一).
- * grads[W]: host array of device pointers, worker w's n gradients of type dt (F16 or
- * BF16). order[W]: host array, order[p] = worker at ring position p (NULL = identity).
+ * grads[W]: host array of device pointers, worker w's n gradients of type dt (F16,
+ * BF16, or F32 for micro-batch sums from zr_accumulate). order[W]: host array,
+ * order[p] = worker at ring position p (NULL = identity).
  * With C = zr_chunk_size(n, W, ZR_ALIGN), block c = [c*C, min((c+1)*C, n)) starts at
  * position c and travels the ring; the result is
  *     sums[i] = (((x_{order[c]}[i] + x_{order[c+1]}[i]) + ...) + x_{order[c+W-1]}[i])
@@ -112,9 +113,19 @@ zr_status zr_bucket_plan(const int64_t* numels, int ntensors, int64_t cap_elems,
  * which ring position (c-1) mod W owns. sums: device, n fp32 (the owners' shards in
  * place). overflow: device int32, set to 1 (never cleared) if any sum is not finite.
  * Errors: ZR_ERR_INVALID for n < 0, W outside [1, ZR_MAX_W], a bad order
- * permutation, null or misaligned pointers, dt not F16/BF16. n == 0 is a no-op. */
+ * permutation, null or misaligned pointers, dt not F16/BF16/F32. n == 0 is a no-op. */
 zr_status zr_reduce_scatter(const void* const* grads, zr_dtype dt, int64_t n, int W, const int* order,
                             float* sums, int32_t* overflow, void* stream);
+
+/* One micro-batch of gradient accumulation on one worker ([P3] Gradient Accumulation:
+ * micro-batch gradients add up locally, with the synchronisation skipped, before the
+ * one reduction of the step): acc[i] = fp32(grad[i]) if `first`, else
+ * acc[i] = acc[i] + fp32(grad[i]) (one fp32 add, round to nearest even).
+ * grad: device, n values of type dt (F16 or BF16); acc: device fp32[n].
+ * Calling it for micro-batches 0..A-1 in order and then zr_reduce_scatter / zr_step
+ * on the fp32 accumulators gives the same bits as the fused A-way step.
+ * Errors: ZR_ERR_INVALID for n < 0, dt not F16/BF16, null or misaligned pointers. */
+zr_status zr_accumulate(const void* grad, zr_dtype dt, float* acc, int64_t n, int first, void* stream);
 
 /* Owner-side update of one shard ([P1] 三: average, convert to FP32 and scale, update
  * m and v, then the FP32 master; [P3] memory table: master, m, v in FP32).
@@ -159,6 +170,8 @@ typedef struct {
     const int64_t* numels;    /* host, definition order */
     const int32_t* order;     /* host [W] ring order, NULL = identity */
     zr_scaler_cfg scaler;
+    int32_t fp32_grads;       /* 1: the gradient replicas are fp32 (e.g. micro-batch sums built with
+                                 zr_accumulate, [P3] Gradient Accumulation); 0: they have `dtype` */
 } zr_plan_desc;
 
 /* Optimizer state and parameter replica, two sets (ping-pong), in the flat layout of

@@ -83,6 +83,8 @@ def lib():
             L.zro_decode.restype = None
             L.zro_encode.argtypes = [ctypes.c_int, vp, vp, i64]
             L.zro_encode.restype = None
+            L.zro_accumulate.argtypes = [ctypes.c_int, vp, vp, i64, ctypes.c_int]
+            L.zro_accumulate.restype = None
             L.zro_ring_reduce_scatter.argtypes = [ctypes.c_int, i64, i64, vp, vp, vp, vp]
             L.zro_ring_reduce_scatter.restype = None
             L.zro_ring_all_gather.argtypes = [ctypes.c_int, i64, i64, vp, vp, vp, vp]
@@ -156,6 +158,13 @@ def encode(dtype: int, x: np.ndarray) -> np.ndarray:
     out = np.empty(x.shape, dtype=np.uint16)
     lib().zro_encode(dtype, _ptr(x), _ptr(out), x.size)
     return out
+
+
+def accumulate(dtype: int, g: np.ndarray, acc: np.ndarray, first: bool) -> None:
+    """In place: acc = fp32(g) if first else acc + fp32(g)."""
+    g = np.ascontiguousarray(g, dtype=np.uint16)
+    assert acc.dtype == np.float32 and acc.flags["C_CONTIGUOUS"] and acc.size == g.size
+    lib().zro_accumulate(dtype, _ptr(g), _ptr(acc), g.size, 1 if first else 0)
 
 
 # ---------------------------------------------------------------- ring

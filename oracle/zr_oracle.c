@@ -141,6 +141,17 @@ void zro_encode(int dtype, const float* in, uint16_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = dtype == ZRO_F16 ? zro_f32_to_f16(in[i]) : zro_f32_to_bf16(in[i]);
 }
 
+/* One micro-batch of gradient accumulation on one worker ([P3] Gradient
+ * Accumulation: the micro-batch gradients are summed locally, the synchronisation
+ * skipped, before the one reduction): acc = fp32(g) for the first micro-batch, then
+ * acc = acc + fp32(g), in micro-batch order. zro_step's S1 is this, A times. */
+void zro_accumulate(int dtype, const uint16_t* g, float* acc, int64_t n, int first) {
+    for (int64_t i = 0; i < n; ++i) {
+        float x = dtype == ZRO_F16 ? zro_f16_to_f32(g[i]) : zro_bf16_to_f32(g[i]);
+        acc[i] = first ? x : acc[i] + x;
+    }
+}
+
 /* ------------------------------------------------------------------------- */
 /* Ring collectives                                                           */
 /* ------------------------------------------------------------------------- */

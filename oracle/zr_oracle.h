@@ -89,6 +89,7 @@ uint16_t zro_f32_to_f16(float x);
 uint16_t zro_f32_to_bf16(float x);
 void zro_decode(int dtype, const uint16_t* in, float* out, int64_t n);
 void zro_encode(int dtype, const float* in, uint16_t* out, int64_t n);
+void zro_accumulate(int dtype, const uint16_t* g, float* acc, int64_t n, int first);
 
 /* ---- ring collectives over one bucket, by ring position ---- */
 void zro_ring_reduce_scatter(int W, int64_t n, int64_t C, float* const* work, float* msg,

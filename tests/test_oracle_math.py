@@ -258,6 +258,34 @@ def test_accumulation_sums_microbatches_first():
     assert W * b * A == len(grads) * b
 
 
+def test_standalone_accumulate_then_ring_equals_step():
+    """zro_accumulate over A micro-batches, then the ring over the fp32 sums, equals the step's own S1 + S2."""
+    W, A, n = 3, 4, 96
+    rng = np.random.default_rng(12)
+    grads = [oracle.encode(oracle.BF16, rng.normal(size=n).astype(F32)) for _ in range(W * A)]
+    zero = np.zeros(n, F32)
+    _, want = oracle.step(W, A, oracle.BF16, np.array([[0, n, 32]]), grads, zero.copy(), zero.copy(), zero.copy(),
+                          np.zeros(n, np.uint16), H, oracle.new_scaler(), want_sums=True)
+    work = []
+    for w in range(W):
+        acc = np.zeros(n, F32)
+        for a in range(A):
+            oracle.accumulate(oracle.BF16, grads[w * A + a], acc, a == 0)
+        work.append(acc)
+    # the accumulators are exactly the left fold of the decoded micro-batches
+    for w in range(W):
+        ref = oracle.decode(oracle.BF16, grads[w * A])
+        for a in range(1, A):
+            ref = (ref + oracle.decode(oracle.BF16, grads[w * A + a])).astype(F32)
+        assert np.array_equal(work[w], ref)
+    oracle.ring_reduce_scatter(work, 32)
+    got = np.empty(n, F32)
+    for p in range(W):
+        c = (p + 1) % W
+        got[c * 32:(c + 1) * 32] = work[p][c * 32:(c + 1) * 32]
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
 def test_sampled_windows_match_full_run():
     """A bucket cut to the same window of every block, run as its own bucket, gives the same values."""
     W, n = 4, 4 * 64

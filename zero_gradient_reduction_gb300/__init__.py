@@ -46,7 +46,7 @@ class PlanDesc(ctypes.Structure):
     _fields_ = [("W", ctypes.c_int32), ("A", ctypes.c_int32), ("dtype", ctypes.c_int), ("stage", ctypes.c_int32),
                 ("align", ctypes.c_int32), ("cap", ctypes.c_int64), ("ntensors", ctypes.c_int32),
                 ("numels", ctypes.POINTER(ctypes.c_int64)), ("order", ctypes.POINTER(ctypes.c_int32)),
-                ("scaler", ScalerCfg)]
+                ("scaler", ScalerCfg), ("fp32_grads", ctypes.c_int32)]
 
 
 class StateC(ctypes.Structure):
@@ -90,6 +90,7 @@ def lib():
                 "zr_adamw_shard_step": (st, [vp, vp, vp, vp, i64, ctypes.POINTER(Hyper), ctypes.c_float, i32, i64,
                                              vp, vp]),
                 "zr_all_gather": (st, [vp, i64, i32, vp, i32, vp]),
+                "zr_accumulate": (st, [vp, i32, vp, i64, i32, vp]),
                 "zr_plan_create": (st, [ctypes.POINTER(PlanDesc), ctypes.POINTER(vp)]),
                 "zr_plan_destroy": (st, [vp]),
                 "zr_plan_numel": (i64, [vp]),
@@ -210,6 +211,12 @@ def adamw_shard_step(shard_sums, m, v, master, hyper: AdamW, loss_scale: float, 
                                      float(loss_scale), int(W), int(t), _ptr(overflow), _stream_handle(stream)))
 
 
+def accumulate(grad, acc, first: bool, n: Optional[int] = None, stream=None) -> None:
+    """acc = fp32(grad) if first else acc + fp32(grad): one micro-batch of gradient accumulation (zr_accumulate)."""
+    n = int(grad.numel()) if n is None else int(n)
+    _check(lib().zr_accumulate(_ptr(grad), _dt_of(grad), _ptr(acc), n, 1 if first else 0, _stream_handle(stream)))
+
+
 def all_gather(master, replicas: Sequence, n: Optional[int] = None, stream=None) -> None:
     n = int(master.numel()) if n is None else int(n)
     arr = _ptr_array(replicas)
@@ -259,7 +266,8 @@ class Plan:
     """A bucketed ZeRO step over W emulated workers (zr_plan_create / zr_step)."""
 
     def __init__(self, numels: Sequence[int], W: int, A: int = 1, dtype: int = BF16, stage: int = 2,
-                 cap: int = 25_000_000, order: Optional[Sequence[int]] = None, scaler: Scaler = Scaler()):
+                 cap: int = 25_000_000, order: Optional[Sequence[int]] = None, scaler: Scaler = Scaler(),
+                 fp32_grads: bool = False):
         self._numels = np.ascontiguousarray(np.asarray(numels, dtype=np.int64))
         self._order = (ctypes.c_int32 * W)(*order) if order is not None else None
         d = PlanDesc()
@@ -268,10 +276,12 @@ class Plan:
         d.numels = self._numels.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
         d.order = ctypes.cast(self._order, ctypes.POINTER(ctypes.c_int32)) if self._order is not None else None
         d.scaler = scaler.c()
+        d.fp32_grads = 1 if fp32_grads else 0
         h = ctypes.c_void_p()
         _check(lib().zr_plan_create(ctypes.byref(d), ctypes.byref(h)))
         self._h = h
         self.W, self.A, self.dtype, self.stage = int(W), int(A), int(dtype), int(stage)
+        self.fp32_grads = bool(fp32_grads)
         self.numel = int(lib().zr_plan_numel(h))
         nb = int(lib().zr_plan_nbuckets(h))
         b = (Bucket * max(nb, 1))()
@@ -286,8 +296,14 @@ class Plan:
         return self._h
 
     def torch_dtype(self):
+        """The parameter replica's torch dtype."""
         import torch
         return torch.float16 if self.dtype == F16 else torch.bfloat16
+
+    def grad_torch_dtype(self):
+        """The gradient replicas' torch dtype (fp32 for a plan over accumulated micro-batches)."""
+        import torch
+        return torch.float32 if self.fp32_grads else self.torch_dtype()
 
     def new_state(self, device="cuda") -> State:
         return State(self.numel, self.torch_dtype(), device)

@@ -50,8 +50,8 @@ __device__ __forceinline__ void block_flag_or(bool mine, int32_t* flag_out) {
 
 // ---------------------------------------------------------------- reduce-scatter
 struct RsArgs {
-  const uint16_t* grads[ZR_MAX_W];  // indexed by worker
-  int order[ZR_MAX_W];              // ring position -> worker
+  const void* grads[ZR_MAX_W];  // indexed by worker
+  int order[ZR_MAX_W];          // ring position -> worker
   float* sums;
   int32_t* overflow;
   int64_t n, C;
@@ -59,7 +59,7 @@ struct RsArgs {
 };
 
 // Ring-order fp32 sum of the W values of element group e (8 elements, or the
-// ragged tail). Block c of the bucket starts at position c.
+// ragged tail). Block c of the bucket starts at position c. DT: input type.
 template <int DT, int WT>
 __global__ void __launch_bounds__(kThreads) rs_kernel(const __grid_constant__ RsArgs a) {
   const int W = WT > 0 ? WT : a.W;
@@ -72,28 +72,26 @@ __global__ void __launch_bounds__(kThreads) rs_kernel(const __grid_constant__ Rs
     if (e + 8 <= a.n) {
       float s[8];
       if (WT > 0) {
-        uint4 raw[WT > 0 ? WT : 1];
+        float xs[WT > 0 ? WT : 1][8];
 #pragma unroll
         for (int h = 0; h < (WT > 0 ? WT : 1); ++h) {
           int pos = c + h;
           pos -= pos >= W ? W : 0;
-          raw[h] = zr::ld_once(a.grads[a.order[pos]] + e);
+          zr::load8<DT>(a.grads[a.order[pos]], e, xs[h]);
         }
-        zr::unpack8<DT>(raw[0], s);
 #pragma unroll
-        for (int h = 1; h < (WT > 0 ? WT : 1); ++h) {
-          float x[8];
-          zr::unpack8<DT>(raw[h], x);
+        for (int j = 0; j < 8; ++j) s[j] = xs[0][j];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x[j]);
-        }
+        for (int h = 1; h < (WT > 0 ? WT : 1); ++h)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], xs[h][j]);
       } else {
-        zr::unpack8<DT>(zr::ld_once(a.grads[a.order[c]] + e), s);
+        zr::load8<DT>(a.grads[a.order[c]], e, s);
         for (int h = 1; h < W; ++h) {
           int pos = c + h;
           pos -= pos >= W ? W : 0;
           float x[8];
-          zr::unpack8<DT>(zr::ld_once(a.grads[a.order[pos]] + e), x);
+          zr::load8<DT>(a.grads[a.order[pos]], e, x);
 #pragma unroll
           for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x[j]);
         }
@@ -104,11 +102,11 @@ __global__ void __launch_bounds__(kThreads) rs_kernel(const __grid_constant__ Rs
       zr::st_once_f4(a.sums + e + 4, make_float4(s[4], s[5], s[6], s[7]));
     } else {
       for (int64_t i = e; i < a.n; ++i) {
-        float s = zr::to_f32<DT>(a.grads[a.order[c]][i]);
+        float s = zr::load1<DT>(a.grads[a.order[c]], i);
         for (int h = 1; h < W; ++h) {
           int pos = c + h;
           pos -= pos >= W ? W : 0;
-          s = __fadd_rn(s, zr::to_f32<DT>(a.grads[a.order[pos]][i]));
+          s = __fadd_rn(s, zr::load1<DT>(a.grads[a.order[pos]], i));
         }
         bad |= zr::nonfinite(s);
         a.sums[i] = s;
@@ -242,7 +240,8 @@ extern "C" zr_status zr_reduce_scatter(const void* const* grads, zr_dtype dt, in
   zr::clear_error();
   if (n < 0) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: n < 0");
   if (W < 1 || W > ZR_MAX_W) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: W=%d outside [1, %d]", W, ZR_MAX_W);
-  if (dt != ZR_F16 && dt != ZR_BF16) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: dtype must be F16 or BF16");
+  if (dt != ZR_F16 && dt != ZR_BF16 && dt != ZR_F32)
+    return fail(ZR_ERR_INVALID, "zr_reduce_scatter: dtype must be F16, BF16 or F32");
   if (!grads || !sums || !overflow) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: null pointer");
   if (!zr::aligned16(sums) || (reinterpret_cast<uintptr_t>(overflow) & 3u))
     return fail(ZR_ERR_INVALID, "zr_reduce_scatter: misaligned output");
@@ -256,7 +255,7 @@ extern "C" zr_status zr_reduce_scatter(const void* const* grads, zr_dtype dt, in
   }
   for (int w = 0; w < W; ++w) {
     if (!grads[w] || !zr::aligned16(grads[w])) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: grads[%d] null or misaligned", w);
-    a.grads[w] = static_cast<const uint16_t*>(grads[w]);
+    a.grads[w] = grads[w];
   }
   if (n == 0) return ZR_OK;
   a.sums = sums;
@@ -267,8 +266,55 @@ extern "C" zr_status zr_reduce_scatter(const void* const* grads, zr_dtype dt, in
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int grid = grid_for((n + 7) / 8);
   if (dt == ZR_F16) launch_rs<zr::DT_F16>(a, grid, s);
-  else launch_rs<zr::DT_BF16>(a, grid, s);
+  else if (dt == ZR_BF16) launch_rs<zr::DT_BF16>(a, grid, s);
+  else launch_rs<zr::DT_F32>(a, grid, s);
   return launch_status("zr_reduce_scatter");
+}
+
+// ---------------------------------------------------------------- accumulate
+namespace {
+template <int DT, bool FIRST>
+__global__ void __launch_bounds__(kThreads) accumulate_kernel(const void* __restrict__ g, float* __restrict__ acc,
+                                                              int64_t n) {
+  const int64_t ngroups = n / 8;
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < ngroups; q += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = q * 8;
+    float x[8];
+    zr::load8<DT>(g, e, x);
+    if (!FIRST) {
+      const float4 a0 = zr::ld_once_f4(acc + e), a1 = zr::ld_once_f4(acc + e + 4);
+      x[0] = __fadd_rn(a0.x, x[0]); x[1] = __fadd_rn(a0.y, x[1]); x[2] = __fadd_rn(a0.z, x[2]);
+      x[3] = __fadd_rn(a0.w, x[3]); x[4] = __fadd_rn(a1.x, x[4]); x[5] = __fadd_rn(a1.y, x[5]);
+      x[6] = __fadd_rn(a1.z, x[6]); x[7] = __fadd_rn(a1.w, x[7]);
+    }
+    zr::st_once_f4(acc + e, make_float4(x[0], x[1], x[2], x[3]));
+    zr::st_once_f4(acc + e + 4, make_float4(x[4], x[5], x[6], x[7]));
+  }
+  for (int64_t i = ngroups * 8 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float x = zr::load1<DT>(g, i);
+    acc[i] = FIRST ? x : __fadd_rn(acc[i], x);
+  }
+}
+}  // namespace
+
+extern "C" zr_status zr_accumulate(const void* grad, zr_dtype dt, float* acc, int64_t n, int first, void* stream) {
+  zr::clear_error();
+  if (n < 0) return fail(ZR_ERR_INVALID, "zr_accumulate: n < 0");
+  if (dt != ZR_F16 && dt != ZR_BF16) return fail(ZR_ERR_INVALID, "zr_accumulate: dtype must be F16 or BF16");
+  if (!grad || !acc || !zr::aligned16(grad) || !zr::aligned16(acc))
+    return fail(ZR_ERR_INVALID, "zr_accumulate: null or misaligned pointer");
+  if (n == 0) return ZR_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int grid = grid_for(n / 8 + 1);
+  if (dt == ZR_F16) {
+    if (first) accumulate_kernel<zr::DT_F16, true><<<grid, kThreads, 0, s>>>(grad, acc, n);
+    else accumulate_kernel<zr::DT_F16, false><<<grid, kThreads, 0, s>>>(grad, acc, n);
+  } else {
+    if (first) accumulate_kernel<zr::DT_BF16, true><<<grid, kThreads, 0, s>>>(grad, acc, n);
+    else accumulate_kernel<zr::DT_BF16, false><<<grid, kThreads, 0, s>>>(grad, acc, n);
+  }
+  return launch_status("zr_accumulate");
 }
 
 extern "C" zr_status zr_adamw_shard_step(const float* shard_sums, float* m, float* v, float* master, int64_t len,

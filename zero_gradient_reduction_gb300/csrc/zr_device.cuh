@@ -9,7 +9,7 @@
 
 namespace zr {
 
-enum { DT_F16 = 0, DT_BF16 = 1 };
+enum { DT_F16 = 0, DT_BF16 = 1, DT_F32 = 2 };
 
 // 16-byte load of data read exactly once: non-coherent path, no L1 allocation,
 // 256-byte L2 prefetch granule. Not volatile, so the compiler may batch loads.
@@ -83,6 +83,25 @@ template <int DT>
 __device__ __forceinline__ uint16_t from_f32(float x) {
   if (DT == DT_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
   return __half_as_ushort(__float2half_rn(x));
+}
+
+// Elements e .. e+7 of an array of type DT (fp16, bf16 or fp32) as 8 fp32 values, exact.
+template <int DT>
+__device__ __forceinline__ void load8(const void* base, int64_t e, float f[8]) {
+  if (DT == DT_F32) {
+    const float* p = static_cast<const float*>(base) + e;
+    const float4 a = ld_once_f4(p), b = ld_once_f4(p + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  } else {
+    unpack8<DT>(ld_once(static_cast<const uint16_t*>(base) + e), f);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ float load1(const void* base, int64_t i) {
+  if (DT == DT_F32) return static_cast<const float*>(base)[i];
+  return to_f32<DT>(static_cast<const uint16_t*>(base)[i]);
 }
 
 __device__ __forceinline__ bool nonfinite(float x) {

@@ -35,6 +35,7 @@ struct zr_plan {
   std::vector<int64_t> tensor_offsets;
   int order[ZR_MAX_W] = {};
   zr_scaler_cfg scaler{};
+  int fp32_grads = 0;  // gradients are fp32 (4 bytes) instead of the param type
   int4* tiles_dev = nullptr;
   int64_t ntiles = 0;
   zr::Ctrl* ctrl_dev = nullptr;
@@ -93,6 +94,7 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   p->stage = d->stage;
   p->align = d->align;
   p->scaler = d->scaler;
+  p->fp32_grads = d->fp32_grads ? 1 : 0;
   bool seen[ZR_MAX_W] = {};
   for (int i = 0; i < d->W; ++i) {
     const int w = d->order ? d->order[i] : i;
@@ -142,7 +144,8 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
     e = cudaMemcpy(p->ctrl_dev, &c, sizeof c, cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) {
-    p->kernel = p->dtype == ZR_F16 ? pick_kernel<zr::DT_F16>(p->W, p->A) : pick_kernel<zr::DT_BF16>(p->W, p->A);
+    const bool f32 = p->fp32_grads != 0;
+    p->kernel = p->dtype == ZR_F16 ? pick_kernel<zr::DT_F16>(p->W, p->A, f32) : pick_kernel<zr::DT_BF16>(p->W, p->A, f32);
     int per_sm = 0, sms = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, p->kernel, kThreads, 0);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
@@ -280,7 +283,7 @@ static zr_status launch_step(zr_plan* p, int stage, const void* const* grads, co
   if (p->ntiles == 0) return ZR_OK;
   FusedArgs a;
   std::memset(&a, 0, sizeof a);
-  for (int r = 0; r < p->W * p->A; ++r) a.grads[r] = static_cast<const uint16_t*>(grads[r]);
+  for (int r = 0; r < p->W * p->A; ++r) a.grads[r] = grads[r];
   for (int i = 0; i < p->W; ++i) a.order[i] = p->order[i];
   a.tiles = p->tiles_dev;
   a.ntiles = p->ntiles;
@@ -351,7 +354,8 @@ extern "C" zr_status zr_step_from_host(zr_plan* p, int stage, const void* const*
   if (s != ZR_OK) return s;
   for (const zr_bucket& b : p->buckets) {
     for (int r = 0; r < R; ++r) {
-      const size_t off = (size_t)b.start * 2, bytes = (size_t)b.len * 2;
+      const size_t esz = p->fp32_grads ? 4 : 2;
+      const size_t off = (size_t)b.start * esz, bytes = (size_t)b.len * esz;
       cudaError_t e = cudaMemcpyAsync(static_cast<char*>(dev_grads[r]) + off,
                                       static_cast<const char*>(host_grads[r]) + off, bytes,
                                       cudaMemcpyHostToDevice, cs);

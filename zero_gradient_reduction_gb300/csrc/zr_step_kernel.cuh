@@ -15,7 +15,7 @@ constexpr int kThreads = 256;
 constexpr int kTileElems = 16384;  // elements per tile (a multiple of 8 * kThreads)
 
 struct FusedArgs {
-  const uint16_t* grads[ZR_MAX_REPLICAS];  // replica w*A + a
+  const void* grads[ZR_MAX_REPLICAS];      // replica w*A + a (16-bit of the param type, or fp32)
   int order[ZR_MAX_W];                     // ring position -> worker
   const int4* tiles;                       // {start lo, start hi, groups, block index c}
   int64_t ntiles;
@@ -114,7 +114,7 @@ __device__ __forceinline__ bool update_group(const FusedArgs& a, const StepConst
 // is uniform over the tile), so tiles need no shared table and no block barrier. For
 // A = 1 with a compile-time W all W gradient loads and the six state loads of a group
 // are issued before any arithmetic.
-template <int DT, int WT, int AT>
+template <int DT, int WT, int AT, int GT>
 __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_constant__ FusedArgs a) {
   __shared__ StepConsts s_k;
   __shared__ int s_bad;
@@ -136,14 +136,14 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
     const int4 d = a.tiles[tile];
     const int64_t start = (int64_t)(((uint64_t)(uint32_t)d.y << 32) | (uint32_t)d.x);
     const int groups = d.z, c = d.w;
-    if (WT > 0 && AT == 1) {
+    if (WT > 0 && AT == 1 && GT == DT) {
       constexpr int WN = WT > 0 ? WT : 1;
       const uint16_t* gp[WN];
 #pragma unroll
       for (int h = 0; h < WN; ++h) {
         int pos = c + h;
         pos -= pos >= WN ? WN : 0;
-        gp[h] = a.grads[a.order[pos]] + start;
+        gp[h] = static_cast<const uint16_t*>(a.grads[a.order[pos]]) + start;
       }
       // U groups per thread and iteration, all of their loads issued before any arithmetic:
       // with few replicas one group holds too few bytes in flight to cover HBM latency.
@@ -191,12 +191,12 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
         for (int h = 0; h < W; ++h) {
           int pos = c + h;
           pos -= pos >= W ? W : 0;
-          const uint16_t* const* rep = a.grads + a.order[pos] * A;  // worker's A micro-batches
+          const void* const* rep = a.grads + a.order[pos] * A;  // worker's A micro-batches
           float w8[8];
-          zr::unpack8<DT>(zr::ld_once(rep[0] + e), w8);
+          zr::load8<GT>(rep[0], e, w8);
           for (int q = 1; q < A; ++q) {
             float x[8];
-            zr::unpack8<DT>(zr::ld_once(rep[q] + e), x);
+            zr::load8<GT>(rep[q], e, x);
 #pragma unroll
             for (int j = 0; j < 8; ++j) w8[j] = __fadd_rn(w8[j], x[j]);
           }
@@ -228,27 +228,29 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
 
 using KernelFn = void (*)(FusedArgs);
 
+// GT: the gradients' type (the param type DT, or fp32 accumulators).
 template <int DT>
-KernelFn pick_kernel(int W, int A) {
+KernelFn pick_kernel(int W, int A, bool fp32_grads) {
+  if (fp32_grads) return A == 1 ? fused_step_kernel<DT, 0, 1, zr::DT_F32> : fused_step_kernel<DT, 0, 0, zr::DT_F32>;
   if (A == 1) {
     switch (W) {
-      case 1: return fused_step_kernel<DT, 1, 1>;
-      case 2: return fused_step_kernel<DT, 2, 1>;
-      case 3: return fused_step_kernel<DT, 3, 1>;
-      case 4: return fused_step_kernel<DT, 4, 1>;
-      case 8: return fused_step_kernel<DT, 8, 1>;
-      default: return fused_step_kernel<DT, 0, 1>;
+      case 1: return fused_step_kernel<DT, 1, 1, DT>;
+      case 2: return fused_step_kernel<DT, 2, 1, DT>;
+      case 3: return fused_step_kernel<DT, 3, 1, DT>;
+      case 4: return fused_step_kernel<DT, 4, 1, DT>;
+      case 8: return fused_step_kernel<DT, 8, 1, DT>;
+      default: return fused_step_kernel<DT, 0, 1, DT>;
     }
   }
   if (A == 4) {
     switch (W) {
-      case 2: return fused_step_kernel<DT, 2, 4>;
-      case 4: return fused_step_kernel<DT, 4, 4>;
-      case 8: return fused_step_kernel<DT, 8, 4>;
-      default: return fused_step_kernel<DT, 0, 4>;
+      case 2: return fused_step_kernel<DT, 2, 4, DT>;
+      case 4: return fused_step_kernel<DT, 4, 4, DT>;
+      case 8: return fused_step_kernel<DT, 8, 4, DT>;
+      default: return fused_step_kernel<DT, 0, 4, DT>;
     }
   }
-  return fused_step_kernel<DT, 0, 0>;
+  return fused_step_kernel<DT, 0, 0, DT>;
 }
 
 }  // namespace
