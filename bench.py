@@ -347,6 +347,65 @@ def run_zr(args, w):
                  "launches_per_step": len(plan.buckets) + 3,
                  "calls": "zr_reduce_scatter per bucket, zr_adamw_shard_step, zr_all_gather"}
         del sums
+    if w.A > 1 and not args.no_chain:
+        # the standalone accumulate path: A zr_accumulate passes per worker into fp32, then the step on the
+        # fp32 sums (W*(2A + 4(A-1) + 4A) + 4W + 26 bytes per param against 2WA + 26 fused)
+        acc_plan = zr.Plan(list(w.tensors), W=w.W, A=1, dtype=w.dtype, stage=w.stage, cap=w.cap,
+                           scaler=zr.Scaler(w.init_scale, w.dynamic), fp32_grads=True)
+        accs = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(w.W)]
+
+        def acc_step():
+            for wk in range(w.W):
+                for q in range(w.A):
+                    zr.accumulate(grads[wk * w.A + q], accs[wk], q == 0, stream=stream)
+            acc_plan.step(accs, state, hyper, stream=stream)
+
+        for _ in range(3):
+            acc_step()
+        torch.cuda.synchronize(dev)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(args.chain_steps):
+            acc_step()
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        acc_ms = c0.elapsed_time(c1) / args.chain_steps
+        acc_bytes = (w.W * (2 * w.A + 4 * (w.A - 1) + 4 * w.A) + 4 * w.W + 26) * plan.n_real
+        chain = {"ms_per_step": acc_ms, "Gparams_per_s": plan.n_real / acc_ms / 1e6,
+                 "alg_bytes_per_param": acc_bytes // plan.n_real, "hbm_GBs": acc_bytes / acc_ms / 1e6,
+                 "launches_per_step": w.W * w.A + 1,
+                 "calls": "zr_accumulate per worker and micro-batch, then zr_step on the fp32 sums"}
+        acc_plan.close()
+        del accs
+
+    # ZeRO-3: the parameter all-gather before each layer's forward/backward, bucket by bucket, from the W
+    # shards into a transient replica (2 bytes read + 2 written per param)
+    zero3 = None
+    if not args.no_chain:
+        shards = plan.new_shards(dev)
+        plan.shard_params(state.param[rep.current], shards, stream=stream)
+        transient = torch.empty_like(state.param[0])
+
+        def gather_all():
+            for b in range(len(plan.buckets)):
+                plan.gather_params(shards, transient, b, b + 1, stream=stream)
+
+        for _ in range(3):
+            gather_all()
+        torch.cuda.synchronize(dev)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(args.chain_steps):
+            gather_all()
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        g_ms = c0.elapsed_time(c1) / args.chain_steps
+        zero3 = {"ms_all_buckets": g_ms, "launches": len(plan.buckets), "hbm_GBs": 4 * plan.numel / g_ms / 1e6,
+                 "frac_of_measured_copy": 4 * plan.numel / g_ms / 1e6 / _peaks()[0],
+                 "call": "zr_gather_params per bucket (the all-gather before each layer's forward and backward)"}
+        del shards, transient
 
     e2e = None
     cpu = None
@@ -388,6 +447,7 @@ def run_zr(args, w):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "unfused_chain": chain,
+        "zero3_param_gather": zero3,
         "gpu_launches": args.steps,
         "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
                    "reasons": clocks.get("reasons"), "samples": clocks.get("samples"),

@@ -264,6 +264,36 @@ zr_status zr_plan_checkpoint(zr_plan* p, void* stream, zr_checkpoint* out);
 zr_status zr_plan_restore(zr_plan* p, const zr_checkpoint* in, void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* ZeRO-3 parameter shards and the all-gather before forward / backward        */
+/* ------------------------------------------------------------------------- */
+
+/* Under ZeRO-3 a worker keeps only its share of the 16-bit parameters and all-gathers
+ * a layer's parameters from the others right before the layer's forward and again
+ * before its backward, dropping them after use ([P1] 四 ZeRO-3: the missing
+ * parameters are broadcast for forward and again for backward, then discarded;
+ * [P2] (13) ②③; [P3] ZeRO Stage 3). Here worker w's shard is the packed
+ * concatenation, in bucket order, of the block it owns in every bucket (the worker at
+ * ring position p owns block (p+1) mod W), zr_plan_shard_numel(w) elements of the
+ * plan's dtype. */
+int64_t zr_plan_shard_numel(const zr_plan* p, int worker);
+/* Where bucket `bucket`'s block starts in worker `worker`'s shard. */
+zr_status zr_plan_shard_offset(const zr_plan* p, int bucket, int worker, int64_t* offset);
+
+/* Copies each worker's owned blocks of the full replica (zr_plan_numel elements of the
+ * plan's dtype, device) into its packed shard: what a ZeRO-3 worker keeps after the
+ * step. shards[W]: host array of device pointers indexed by worker id.
+ * Errors: ZR_ERR_INVALID for null or misaligned pointers; ZR_ERR_CUDA. */
+zr_status zr_shard_params(zr_plan* p, const void* replica, void* const* shards, void* stream);
+
+/* The ZeRO-3 parameter all-gather for buckets [bucket_lo, bucket_hi): every block of
+ * those buckets is copied from its owner's shard into the (transient) replica at its
+ * flat position; the rest of the replica is not touched. Moves 2 bytes in and 2 out
+ * per parameter. Errors: ZR_ERR_INVALID for a bad range, null or misaligned
+ * pointers; ZR_ERR_CUDA. */
+zr_status zr_gather_params(zr_plan* p, int bucket_lo, int bucket_hi, const void* const* shards, void* replica,
+                           void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* Fused step without device allocation                                        */
 /* ------------------------------------------------------------------------- */
 

@@ -85,6 +85,11 @@ def lib():
             L.zro_encode.restype = None
             L.zro_accumulate.argtypes = [ctypes.c_int, vp, vp, i64, ctypes.c_int]
             L.zro_accumulate.restype = None
+            L.zro_shard_params.argtypes = [ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]
+            L.zro_shard_params.restype = None
+            L.zro_param_all_gather.argtypes = [ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, vp,
+                                               vp]
+            L.zro_param_all_gather.restype = ctypes.c_int
             L.zro_ring_reduce_scatter.argtypes = [ctypes.c_int, i64, i64, vp, vp, vp, vp]
             L.zro_ring_reduce_scatter.restype = None
             L.zro_ring_all_gather.argtypes = [ctypes.c_int, i64, i64, vp, vp, vp, vp]
@@ -203,6 +208,41 @@ def ring_all_gather(reps: List[np.ndarray], C: int, hops: Optional[range] = None
         lib().zro_ring_all_gather_hops(W, n, int(C), ctypes.addressof(ptrs), _ptr(msg), _ptr(sent), _ptr(recv),
                                        hops.start, hops.stop)
     return sent, recv
+
+
+def shard_sizes(buckets: np.ndarray, W: int, order: Optional[Sequence[int]] = None) -> List[int]:
+    """Elements of each worker's ZeRO-3 shard: the sum of its owned block over the buckets."""
+    order = list(order) if order is not None else list(range(W))
+    sizes = [0] * W
+    for _, n, C in np.asarray(buckets).reshape(-1, 3):
+        for p in range(W):
+            c = (p + 1) % W
+            sizes[order[p]] += max(0, min(int(n), (c + 1) * int(C)) - min(int(n), c * int(C)))
+    return sizes
+
+
+def shard_params(W: int, buckets: np.ndarray, replica: np.ndarray, order: Optional[Sequence[int]] = None):
+    """Per-worker ZeRO-3 shards of a full 16-bit replica (list indexed by worker id)."""
+    shards = [np.zeros(max(s, 1), np.uint16) for s in shard_sizes(buckets, W, order)]
+    bk, nb = _buckets_struct(buckets)
+    ordc = (ctypes.c_int * W)(*(order if order is not None else range(W)))
+    ptrs = (ctypes.c_void_p * W)(*[_ptr(s) for s in shards])
+    rep = np.ascontiguousarray(replica, dtype=np.uint16)
+    lib().zro_shard_params(W, ctypes.addressof(ordc), nb, ctypes.addressof(bk), _ptr(rep), ctypes.addressof(ptrs))
+    return shards
+
+
+def param_all_gather(W: int, buckets: np.ndarray, shards: List[np.ndarray], replica: np.ndarray, b_lo: int, b_hi: int,
+                     order: Optional[Sequence[int]] = None) -> None:
+    """In place on `replica`: the ring all-gather of buckets [b_lo, b_hi) from the shards."""
+    bk, nb = _buckets_struct(buckets)
+    ordc = (ctypes.c_int * W)(*(order if order is not None else range(W)))
+    ptrs = (ctypes.c_void_p * W)(*[_ptr(s) for s in shards])
+    assert replica.dtype == np.uint16 and replica.flags["C_CONTIGUOUS"]
+    rc = lib().zro_param_all_gather(W, ctypes.addressof(ordc), nb, ctypes.addressof(bk), int(b_lo), int(b_hi),
+                                    ctypes.addressof(ptrs), _ptr(replica))
+    if rc != 0:
+        raise RuntimeError(f"zro_param_all_gather rc={rc}")
 
 
 def ring_traffic(n: int, W: int, align: int = 8):

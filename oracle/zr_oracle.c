@@ -223,6 +223,70 @@ void zro_ring_all_gather(int W, int64_t n, int64_t C, uint16_t* const* rep, uint
     zro_ring_all_gather_hops(W, n, C, rep, msg, sent, recv, 0, W - 1);
 }
 
+/* ZeRO-3 keeps on each worker only its share of the 16-bit parameters ([P1] 四:
+ * parameters are partitioned too; [P3] ZeRO Stage 3: each GPU stores 1/W of them).
+ * Reading: the worker at ring position p keeps the block it owns after the
+ * reduce-scatter, (p+1) mod W, of every bucket, packed in bucket order.
+ * shards[w] is indexed by worker id. */
+void zro_shard_params(int W, const int* order, int nbuckets, const zro_bucket* buckets, const uint16_t* replica,
+                      uint16_t* const* shards) {
+    int64_t fill[ZRO_MAX_W] = {0};
+    for (int b = 0; b < nbuckets; ++b) {
+        const int64_t st = buckets[b].start, n = buckets[b].len, C = buckets[b].chunk;
+        for (int p = 0; p < W; ++p) {
+            const int w = order ? order[p] : p;
+            const int c = mod(p + 1, W);
+            const int64_t lo = chunk_lo(n, C, c), hi = chunk_hi(n, C, c);
+            memcpy(shards[w] + fill[w], replica + st + lo, (size_t)(hi - lo) * sizeof(uint16_t));
+            fill[w] += hi - lo;
+        }
+    }
+}
+
+/* The parameter all-gather that ZeRO-3 runs before a layer's forward and again before
+ * its backward ([P1] 四; [P2] (13) ②③): for each bucket in [b_lo, b_hi), every
+ * position starts with its own block taken from its shard, the W-1 ring all-gather
+ * hops run, all W replicas must agree, and the result is written to `replica` at the
+ * bucket's flat position. Returns 0, -2 on allocation failure, -3 on disagreement. */
+int zro_param_all_gather(int W, const int* order, int nbuckets, const zro_bucket* buckets, int b_lo, int b_hi,
+                         const uint16_t* const* shards, uint16_t* replica) {
+    int64_t maxlen = 0, maxC = 0;
+    for (int b = 0; b < nbuckets; ++b) {
+        if (buckets[b].len > maxlen) maxlen = buckets[b].len;
+        if (buckets[b].chunk > maxC) maxC = buckets[b].chunk;
+    }
+    uint16_t* rep[ZRO_MAX_W];
+    uint16_t* msg = (uint16_t*)malloc((size_t)(W * (maxC ? maxC : 1)) * sizeof(uint16_t));
+    int rc = msg ? 0 : -2;
+    for (int p = 0; p < W; ++p) {
+        rep[p] = (uint16_t*)calloc((size_t)(maxlen ? maxlen : 1), sizeof(uint16_t));
+        if (!rep[p]) rc = -2;
+    }
+    int64_t off[ZRO_MAX_W] = {0};  /* running offset of each worker's shard, by worker id */
+    for (int b = 0; b < nbuckets && rc == 0; ++b) {
+        const int64_t st = buckets[b].start, n = buckets[b].len, C = buckets[b].chunk;
+        for (int p = 0; p < W; ++p) {
+            const int w = order ? order[p] : p;
+            const int c = mod(p + 1, W);
+            const int64_t lo = chunk_lo(n, C, c), hi = chunk_hi(n, C, c);
+            if (b >= b_lo && b < b_hi) {
+                memset(rep[p], 0, (size_t)n * sizeof(uint16_t));
+                memcpy(rep[p] + lo, shards[w] + off[w], (size_t)(hi - lo) * sizeof(uint16_t));
+            }
+            off[w] += hi - lo;
+        }
+        if (b < b_lo || b >= b_hi) continue;
+        int64_t sent[ZRO_MAX_W] = {0}, recv[ZRO_MAX_W] = {0};
+        zro_ring_all_gather(W, n, C, rep, msg, sent, recv);
+        for (int p = 1; p < W; ++p)
+            if (memcmp(rep[p], rep[0], (size_t)n * sizeof(uint16_t)) != 0) rc = -3;
+        memcpy(replica + st, rep[0], (size_t)n * sizeof(uint16_t));
+    }
+    for (int p = 0; p < W; ++p) free(rep[p]);
+    free(msg);
+    return rc;
+}
+
 /* Per-position traffic of one ring phase over an n-element bucket, by running
  * the hop schedule on block sizes only. */
 void zro_ring_traffic(int64_t n, int W, int align, int64_t* sent_per_pos, int64_t* recv_per_pos) {

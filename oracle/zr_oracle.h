@@ -102,6 +102,12 @@ void zro_ring_all_gather(int W, int64_t n, int64_t C, uint16_t* const* rep, uint
                          int64_t* sent, int64_t* recv);
 void zro_ring_traffic(int64_t n, int W, int align, int64_t* sent_per_pos, int64_t* recv_per_pos);
 
+/* ---- ZeRO-3 parameter shards and the all-gather before forward/backward ---- */
+void zro_shard_params(int W, const int* order, int nbuckets, const zro_bucket* buckets, const uint16_t* replica,
+                      uint16_t* const* shards);
+int zro_param_all_gather(int W, const int* order, int nbuckets, const zro_bucket* buckets, int b_lo, int b_hi,
+                         const uint16_t* const* shards, uint16_t* replica);
+
 /* ---- per-shard arithmetic ---- */
 float zro_unscale_factor(float scale, int W);
 float zro_bias_correction(float beta, int64_t t);

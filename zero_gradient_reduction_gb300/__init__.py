@@ -91,6 +91,10 @@ def lib():
                                              vp, vp]),
                 "zr_all_gather": (st, [vp, i64, i32, vp, i32, vp]),
                 "zr_accumulate": (st, [vp, i32, vp, i64, i32, vp]),
+                "zr_plan_shard_numel": (i64, [vp, i32]),
+                "zr_plan_shard_offset": (st, [vp, i32, i32, ctypes.POINTER(ctypes.c_int64)]),
+                "zr_shard_params": (st, [vp, vp, vp, vp]),
+                "zr_gather_params": (st, [vp, i32, i32, vp, vp, vp]),
                 "zr_plan_create": (st, [ctypes.POINTER(PlanDesc), ctypes.POINTER(vp)]),
                 "zr_plan_destroy": (st, [vp]),
                 "zr_plan_numel": (i64, [vp]),
@@ -335,6 +339,33 @@ class Plan:
         rep = StepReport()
         _check(lib().zr_plan_report(self._h, _stream_handle(stream), ctypes.byref(rep)))
         return rep
+
+    # ---- ZeRO-3 parameter shards
+    def shard_numel(self, worker: int) -> int:
+        return int(lib().zr_plan_shard_numel(self._h, int(worker)))
+
+    def shard_offset(self, bucket: int, worker: int) -> int:
+        off = ctypes.c_int64()
+        _check(lib().zr_plan_shard_offset(self._h, int(bucket), int(worker), ctypes.byref(off)))
+        return int(off.value)
+
+    def new_shards(self, device="cuda"):
+        import torch
+        return [torch.empty(max(self.shard_numel(w), 8), dtype=self.torch_dtype(), device=device)
+                for w in range(self.W)]
+
+    def shard_params(self, replica, shards: Sequence, stream=None) -> None:
+        """Each worker keeps its owned blocks of the full replica (zr_shard_params)."""
+        arr = _ptr_array(shards)
+        _check(lib().zr_shard_params(self._h, _ptr(replica), ctypes.addressof(arr), _stream_handle(stream)))
+
+    def gather_params(self, shards: Sequence, replica, bucket_lo: int = 0, bucket_hi: Optional[int] = None,
+                      stream=None) -> None:
+        """ZeRO-3 all-gather of buckets [bucket_lo, bucket_hi) into the transient replica (zr_gather_params)."""
+        hi = len(self.buckets) if bucket_hi is None else int(bucket_hi)
+        arr = _ptr_array(shards)
+        _check(lib().zr_gather_params(self._h, int(bucket_lo), hi, ctypes.addressof(arr), _ptr(replica),
+                                      _stream_handle(stream)))
 
     def checkpoint(self, stream=None) -> Checkpoint:
         """The control block's step state (live set, scale, t, ...); save the live state tensors with it."""

@@ -19,10 +19,10 @@ OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libzr.so")
 ARCH = os.environ.get("ZR_CUDA_ARCH", "103a")
 
-CU = ["zr_step.cu", "zr_collectives.cu", "zr_noalloc.cu"]
+CU = ["zr_step.cu", "zr_collectives.cu", "zr_noalloc.cu", "zr_zero3.cu"]
 CPP = ["zr_host.cpp"]
 HEADERS = [os.path.join(INCLUDE, "zr.h"), os.path.join(CSRC, "zr_internal.h"), os.path.join(CSRC, "zr_device.cuh"),
-           os.path.join(CSRC, "zr_step_kernel.cuh")]
+           os.path.join(CSRC, "zr_step_kernel.cuh"), os.path.join(CSRC, "zr_plan.h")]
 
 
 def _nvcc_flags(verbose_ptxas: bool = False):

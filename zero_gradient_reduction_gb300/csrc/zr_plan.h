@@ -1,0 +1,42 @@
+// The plan object behind the zr_plan handle (host side, internal to libzr).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <vector>
+
+#include "zr_internal.h"
+
+struct zr_plan {
+  int W = 0, A = 0, stage = 0, align = 0;
+  zr_dtype dtype = ZR_BF16;
+  int64_t numel = 0, n_real = 0;
+  std::vector<zr_bucket> buckets;
+  std::vector<int64_t> tensor_offsets;
+  int order[ZR_MAX_W] = {};
+  zr_scaler_cfg scaler{};
+  int fp32_grads = 0;  // gradients are fp32 (4 bytes) instead of the param type
+  // fused step: tile schedule, control block, kernel and grid
+  int4* tiles_dev = nullptr;
+  int64_t ntiles = 0;
+  zr::Ctrl* ctrl_dev = nullptr;
+  void* kernel = nullptr;  // the fused_step_kernel instantiation for (dtype, W, A)
+  int grid = 0;
+  int device = 0;
+  // ZeRO-3 parameter shards: the worker at ring position p keeps block (p+1) mod W of
+  // every bucket, packed in bucket order. shard_off[b*W + w] is where bucket b's block
+  // starts in worker w's shard; the shard tile table cuts every (bucket, block) piece
+  // into copies of at most 16K elements (two int4 per tile: {flat lo, flat hi, shard lo,
+  // shard hi}, {groups of 8, worker, 0, 0}); bucket b's tiles are
+  // [shard_tile_begin[b], shard_tile_begin[b+1]).
+  std::vector<int64_t> shard_numel;
+  std::vector<int64_t> shard_off;
+  std::vector<int64_t> shard_tile_begin;
+  int4* shard_tiles_dev = nullptr;
+  int64_t nshard_tiles = 0;
+};
+
+namespace zr {
+// Builds the ZeRO-3 shard bookkeeping and its device tile table (zr_zero3.cu).
+zr_status build_shard_tables(zr_plan* p);
+}  // namespace zr

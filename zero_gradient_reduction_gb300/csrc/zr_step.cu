@@ -25,24 +25,8 @@ namespace zr {
 float bias_correction_host(float beta, int64_t t);
 }
 
+#include "zr_plan.h"
 #include "zr_step_kernel.cuh"
-
-struct zr_plan {
-  int W = 0, A = 0, stage = 0, align = 0;
-  zr_dtype dtype = ZR_BF16;
-  int64_t numel = 0, n_real = 0;
-  std::vector<zr_bucket> buckets;
-  std::vector<int64_t> tensor_offsets;
-  int order[ZR_MAX_W] = {};
-  zr_scaler_cfg scaler{};
-  int fp32_grads = 0;  // gradients are fp32 (4 bytes) instead of the param type
-  int4* tiles_dev = nullptr;
-  int64_t ntiles = 0;
-  zr::Ctrl* ctrl_dev = nullptr;
-  KernelFn kernel = nullptr;
-  int grid = 0;
-  int device = 0;
-};
 
 namespace {
 
@@ -145,9 +129,10 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   }
   if (e == cudaSuccess) {
     const bool f32 = p->fp32_grads != 0;
-    p->kernel = p->dtype == ZR_F16 ? pick_kernel<zr::DT_F16>(p->W, p->A, f32) : pick_kernel<zr::DT_BF16>(p->W, p->A, f32);
+    KernelFn k = p->dtype == ZR_F16 ? pick_kernel<zr::DT_F16>(p->W, p->A, f32) : pick_kernel<zr::DT_BF16>(p->W, p->A, f32);
+    p->kernel = reinterpret_cast<void*>(k);
     int per_sm = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, p->kernel, kThreads, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, 0);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
     if (e == cudaSuccess) {
       if (per_sm < 1) per_sm = 1;
@@ -160,6 +145,11 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
     zr_plan_destroy(p);
     return s;
   }
+  zr_status ss = zr::build_shard_tables(p);
+  if (ss != ZR_OK) {
+    zr_plan_destroy(p);
+    return ss;
+  }
   *out = p;
   return ZR_OK;
 }
@@ -168,6 +158,7 @@ extern "C" zr_status zr_plan_destroy(zr_plan* p) {
   if (!p) return ZR_OK;
   if (p->tiles_dev) cudaFree(p->tiles_dev);
   if (p->ctrl_dev) cudaFree(p->ctrl_dev);
+  if (p->shard_tiles_dev) cudaFree(p->shard_tiles_dev);
   delete p;
   return ZR_OK;
 }
@@ -302,7 +293,7 @@ static zr_status launch_step(zr_plan* p, int stage, const void* const* grads, co
   a.W = p->W;
   a.A = p->A;
   a.stage = stage;
-  p->kernel<<<p->grid, kThreads, 0, s>>>(a);
+  reinterpret_cast<KernelFn>(p->kernel)<<<p->grid, kThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ZR_OK : fail(ZR_ERR_CUDA, "zr_step: launch failed: %s", cudaGetErrorString(e));
 }
