@@ -235,6 +235,62 @@ def _config(w, buckets, l2_note):
             "alg_bytes_per_param": w.alg_bytes_per_param(), "l2": l2_note, "parallelism": "replicas"}
 
 
+def measure_overlap(torch, zr, plan, grads, state, hyper, dev, stream, tokens: int = 8192, reps: int = 3):
+    """Bucketed overlap against a synthetic backward: on a compute stream, bucket b's "backward" is a bf16 GEMM
+    of about 4 * tokens * n_b FLOPs (weight and input gradients of n_b parameters), after which an event marks
+    the bucket's gradients ready and zr_step_bucket(b) runs on a side stream. Compared with backward followed by
+    the one-launch step."""
+    K = 2048
+    ns = [max(1, int(round(4 * tokens * int(n_b) / (2 * tokens * K)))) for _, n_b, _ in plan.buckets]
+    a_mat = torch.randn(tokens, K, device=dev, dtype=torch.bfloat16)
+    b_flat = torch.randn(K * max(ns), device=dev, dtype=torch.bfloat16)
+    c_flat = torch.empty(tokens * max(ns), device=dev, dtype=torch.bfloat16)
+    # the bucket steps get the higher priority, so a ready bucket is scheduled as soon as SMs free up
+    # (torch maps an out-of-range priority to the nearest valid one; lower numbers are higher priority)
+    compute = torch.cuda.Stream(dev, priority=0)
+    side = torch.cuda.Stream(dev, priority=-100)
+
+    def backward(events=None):
+        with torch.cuda.stream(compute):
+            for b, nb in enumerate(ns):
+                torch.matmul(a_mat, b_flat[:K * nb].view(K, nb), out=c_flat[:tokens * nb].view(tokens, nb))
+                if events is not None:
+                    events[b].record(compute)
+
+    def timed(fn):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize(dev)
+        return (time.perf_counter() - t0) / reps * 1e3
+
+    def serial():
+        backward()
+        stream.wait_stream(compute)
+        plan.step(grads, state, hyper, stream=stream)
+        compute.wait_stream(stream)
+
+    def overlapped():
+        events = [torch.cuda.Event() for _ in ns]
+        side.wait_stream(compute)
+        backward(events)
+        plan.step_overlapped(grads, state, hyper, events, side)
+        compute.wait_stream(side)
+
+    def step_only():
+        plan.step(grads, state, hyper, stream=stream)
+
+    for fn in (backward, step_only, serial, overlapped):
+        fn()
+    t_bwd, t_step = timed(backward), timed(step_only)
+    t_serial, t_over = timed(serial), timed(overlapped)
+    return {"backward_ms": t_bwd, "step_ms": t_step, "serial_ms": t_serial, "overlapped_ms": t_over,
+            "hidden_fraction_of_step": (t_serial - t_over) / t_step if t_step > 0 else None,
+            "synthetic_backward": f"bf16 GEMM {tokens} x {K} x n_b/1024 per bucket (~4*{tokens}*n_b FLOPs)",
+            "api": "zr_step_bucket per bucket on a side stream after the bucket's ready event"}
+
+
 def run_zr(args, w):
     import torch
     ws, rank, local = _dist_env()
@@ -407,6 +463,10 @@ def run_zr(args, w):
                  "call": "zr_gather_params per bucket (the all-gather before each layer's forward and backward)"}
         del shards, transient
 
+    overlap = None
+    if not args.no_chain and w.A == 1:
+        overlap = measure_overlap(torch, zr, plan, grads, state, hyper, dev, stream)
+
     e2e = None
     cpu = None
     if not args.no_e2e:
@@ -448,6 +508,7 @@ def run_zr(args, w):
         "e2e": e2e,
         "unfused_chain": chain,
         "zero3_param_gather": zero3,
+        "bucketed_overlap": overlap,
         "gpu_launches": args.steps,
         "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
                    "reasons": clocks.get("reasons"), "samples": clocks.get("samples"),

@@ -241,6 +241,19 @@ zr_status zr_step(zr_plan* p, int stage, const void* const* grads, const zr_stat
 zr_status zr_step_from_host(zr_plan* p, int stage, const void* const* host_grads, void* const* dev_grads,
                             const zr_state* st, const zr_adamw_hyper* h, void* stream, zr_step_report* rep);
 
+/* One bucket of a step, for overlap with backward ([P1] 二: a bucket is synchronised as
+ * soon as all its gradients exist, while the GPU keeps computing the others; [P3] DDP
+ * Gradient Bucketing and Overlap). Call it once for every bucket b = 0 .. nbuckets-1,
+ * in that order (bucket 0 holds the output-side layers, whose gradients come first),
+ * each launch ordered after the one before (one stream, or events), typically as bucket
+ * b's gradients become ready. The launches together compute exactly what one zr_step
+ * computes: the last block of the last launch takes the overflow decision for the whole
+ * step and commits. A step must launch every bucket exactly once; after an incomplete
+ * step, call zr_plan_reset. Same arguments and errors as zr_step, plus ZR_ERR_INVALID
+ * for a bucket index outside [0, nbuckets). */
+zr_status zr_step_bucket(zr_plan* p, int stage, int bucket, const void* const* grads, const zr_state* st,
+                         const zr_adamw_hyper* h, void* stream);
+
 /* Synchronises `stream` and reads the control block into *rep. */
 zr_status zr_plan_report(zr_plan* p, void* stream, zr_step_report* rep);
 

@@ -91,6 +91,7 @@ def lib():
                                              vp, vp]),
                 "zr_all_gather": (st, [vp, i64, i32, vp, i32, vp]),
                 "zr_accumulate": (st, [vp, i32, vp, i64, i32, vp]),
+                "zr_step_bucket": (st, [vp, i32, i32, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp]),
                 "zr_plan_shard_numel": (i64, [vp, i32]),
                 "zr_plan_shard_offset": (st, [vp, i32, i32, ctypes.POINTER(ctypes.c_int64)]),
                 "zr_shard_params": (st, [vp, vp, vp, vp]),
@@ -322,6 +323,24 @@ class Plan:
                              ctypes.byref(st), ctypes.byref(h), _stream_handle(stream),
                              ctypes.byref(rep) if rep is not None else None))
         return rep
+
+    def step_bucket(self, bucket: int, grads: Sequence, state: State, hyper: AdamW, stage: Optional[int] = None,
+                    stream=None) -> None:
+        """One bucket of a step (zr_step_bucket): call for buckets 0..nb-1 in order; the last commits."""
+        arr = _ptr_array(grads)
+        st = state.c()
+        h = hyper.c()
+        _check(lib().zr_step_bucket(self._h, int(stage if stage is not None else self.stage), int(bucket),
+                                    ctypes.addressof(arr), ctypes.byref(st), ctypes.byref(h), _stream_handle(stream)))
+
+    def step_overlapped(self, grads: Sequence, state: State, hyper: AdamW, ready_events: Sequence, side_stream,
+                        stage: Optional[int] = None) -> None:
+        """Bucketed overlap with backward: ready_events[b] is recorded (on the compute stream) when bucket b's
+        gradients exist; bucket b's step then runs on side_stream after that event, while backward continues."""
+        assert len(ready_events) == len(self.buckets)
+        for b, ev in enumerate(ready_events):
+            side_stream.wait_event(ev)
+            self.step_bucket(b, grads, state, hyper, stage=stage, stream=side_stream)
 
     def step_from_host(self, host_grads: Sequence, dev_grads: Sequence, state: State, hyper: AdamW,
                        stage: Optional[int] = None, stream=None) -> StepReport:

@@ -23,6 +23,11 @@ struct zr_plan {
   void* kernel = nullptr;  // the fused_step_kernel instantiation for (dtype, W, A)
   int grid = 0;
   int device = 0;
+  // bucketed launches (zr_step_bucket): bucket b's tiles are [tile_begin[b], tile_begin[b+1]),
+  // launched with bucket_grid[b] blocks; a step's launches add up to bucket_blocks blocks
+  std::vector<int64_t> tile_begin;
+  std::vector<int> bucket_grid;
+  unsigned bucket_blocks = 0;
   // ZeRO-3 parameter shards: the worker at ring position p keeps block (p+1) mod W of
   // every bucket, packed in bucket order. shard_off[b*W + w] is where bucket b's block
   // starts in worker w's shard; the shard tile table cuts every (bucket, block) piece

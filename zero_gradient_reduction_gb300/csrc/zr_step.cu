@@ -106,6 +106,7 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   // Tile schedule: every block of every bucket cut into pieces of at most kTileElems.
   std::vector<int4> tiles;
   for (const zr_bucket& b : p->buckets) {
+    p->tile_begin.push_back((int64_t)tiles.size());
     for (int c = 0; c < p->W; ++c) {
       int64_t lo = b.start + (int64_t)c * b.chunk, hi = lo + b.chunk;
       const int64_t end = b.start + b.len;
@@ -118,6 +119,7 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
     }
   }
   p->ntiles = (int64_t)tiles.size();
+  p->tile_begin.push_back(p->ntiles);
   cudaError_t e = cudaGetDevice(&p->device);
   if (e == cudaSuccess && !tiles.empty()) e = cudaMalloc(&p->tiles_dev, tiles.size() * sizeof(int4));
   if (e == cudaSuccess && !tiles.empty())
@@ -138,6 +140,11 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
       if (per_sm < 1) per_sm = 1;
       const int64_t full = (int64_t)sms * per_sm;
       p->grid = (int)(p->ntiles < full ? (p->ntiles > 0 ? p->ntiles : 1) : full);
+      for (size_t b = 0; b + 1 < p->tile_begin.size(); ++b) {
+        const int64_t nt = p->tile_begin[b + 1] - p->tile_begin[b];
+        p->bucket_grid.push_back((int)(nt < full ? nt : full));
+        p->bucket_blocks += (unsigned)p->bucket_grid.back();
+      }
     }
   }
   if (e != cudaSuccess) {
@@ -269,15 +276,20 @@ static zr_status check_step_args(const zr_plan* p, int stage, const void* const*
   return ZR_OK;
 }
 
+// One launch of the fused kernel over tiles [tile0, tile1) with `grid` blocks; the step's
+// launches add up to `total` blocks, and the last of those blocks decides the step.
 static zr_status launch_step(zr_plan* p, int stage, const void* const* grads, const zr_state* st,
-                             const zr_adamw_hyper* h, cudaStream_t s) {
-  if (p->ntiles == 0) return ZR_OK;
+                             const zr_adamw_hyper* h, cudaStream_t s, int64_t tile0, int64_t tile1, int grid,
+                             unsigned total) {
+  if (tile1 <= tile0 || grid < 1) return ZR_OK;
   FusedArgs a;
   std::memset(&a, 0, sizeof a);
   for (int r = 0; r < p->W * p->A; ++r) a.grads[r] = grads[r];
   for (int i = 0; i < p->W; ++i) a.order[i] = p->order[i];
   a.tiles = p->tiles_dev;
-  a.ntiles = p->ntiles;
+  a.tile0 = tile0;
+  a.tile1 = tile1;
+  a.total_blocks = total;
   for (int k = 0; k < 2; ++k) {
     a.master[k] = st->master[k];
     a.m[k] = st->m[k];
@@ -293,7 +305,7 @@ static zr_status launch_step(zr_plan* p, int stage, const void* const* grads, co
   a.W = p->W;
   a.A = p->A;
   a.stage = stage;
-  reinterpret_cast<KernelFn>(p->kernel)<<<p->grid, kThreads, 0, s>>>(a);
+  reinterpret_cast<KernelFn>(p->kernel)<<<grid, kThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ZR_OK : fail(ZR_ERR_CUDA, "zr_step: launch failed: %s", cudaGetErrorString(e));
 }
@@ -304,9 +316,20 @@ extern "C" zr_status zr_step(zr_plan* p, int stage, const void* const* grads, co
   zr_status s = check_step_args(p, stage, grads, st, h);
   if (s != ZR_OK) return s;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  s = launch_step(p, stage, grads, st, h, cs);
+  s = launch_step(p, stage, grads, st, h, cs, 0, p->ntiles, p->grid, (unsigned)p->grid);
   if (s != ZR_OK || !rep) return s;
   return zr_plan_report(p, stream, rep);
+}
+
+extern "C" zr_status zr_step_bucket(zr_plan* p, int stage, int bucket, const void* const* grads, const zr_state* st,
+                                    const zr_adamw_hyper* h, void* stream) {
+  zr::clear_error();
+  zr_status s = check_step_args(p, stage, grads, st, h);
+  if (s != ZR_OK) return s;
+  if (bucket < 0 || bucket >= (int)p->buckets.size())
+    return fail(ZR_ERR_INVALID, "zr_step_bucket: bucket %d outside [0, %d)", bucket, (int)p->buckets.size());
+  return launch_step(p, stage, grads, st, h, static_cast<cudaStream_t>(stream), p->tile_begin[bucket],
+                     p->tile_begin[bucket + 1], p->bucket_grid[bucket], p->bucket_blocks);
 }
 
 extern "C" zr_status zr_step_from_host(zr_plan* p, int stage, const void* const* host_grads, void* const* dev_grads,
@@ -337,7 +360,7 @@ extern "C" zr_status zr_step_from_host(zr_plan* p, int stage, const void* const*
   if (direct) {
     zr_status s = check_step_args(p, stage, mapped, st, h);
     if (s != ZR_OK) return s;
-    s = launch_step(p, stage, mapped, st, h, cs);
+    s = launch_step(p, stage, mapped, st, h, cs, 0, p->ntiles, p->grid, (unsigned)p->grid);
     if (s != ZR_OK) return s;
     return zr_plan_report(p, stream, rep);
   }
@@ -353,7 +376,8 @@ extern "C" zr_status zr_step_from_host(zr_plan* p, int stage, const void* const*
       if (e != cudaSuccess) return cuda_fail("zr_step_from_host: copy", e);
     }
   }
-  s = launch_step(p, stage, const_cast<const void* const*>(dev_grads), st, h, cs);
+  s = launch_step(p, stage, const_cast<const void* const*>(dev_grads), st, h, cs, 0, p->ntiles, p->grid,
+                  (unsigned)p->grid);
   if (s != ZR_OK) return s;
   return zr_plan_report(p, stream, rep);
 }

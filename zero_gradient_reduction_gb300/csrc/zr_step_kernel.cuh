@@ -18,7 +18,8 @@ struct FusedArgs {
   const void* grads[ZR_MAX_REPLICAS];      // replica w*A + a (16-bit of the param type, or fp32)
   int order[ZR_MAX_W];                     // ring position -> worker
   const int4* tiles;                       // {start lo, start hi, groups, block index c}
-  int64_t ntiles;
+  int64_t tile0, tile1;                    // this launch's tiles: [tile0, tile1)
+  unsigned total_blocks;                   // blocks over all launches of the step (one, or one per bucket)
   float* master[2];
   float* m[2];
   float* v[2];
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
   const float* __restrict__ v_in = a.v[K.cur];
   bool bad = false;
 
-  for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+  for (int64_t tile = a.tile0 + blockIdx.x; tile < a.tile1; tile += gridDim.x) {
     const int4 d = a.tiles[tile];
     const int64_t start = (int64_t)(((uint64_t)(uint32_t)d.y << 32) | (uint32_t)d.x);
     const int groups = d.z, c = d.w;
@@ -211,7 +212,8 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
     }
   }
 
-  // Block flag -> control block, then the ticket: the last block to arrive decides.
+  // Block flag -> control block, then the ticket: the last block to arrive, over all
+  // launches of the step, decides.
   if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0) s_bad = 1;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
     s_ticket = atomicAdd(&a.ctrl->ticket, 1u);
   }
   __syncthreads();
-  if (s_ticket == gridDim.x - 1 && threadIdx.x == 0) {
+  if (s_ticket == a.total_blocks - 1 && threadIdx.x == 0) {
     __threadfence();
     finish_step(a);
   }
