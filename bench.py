@@ -467,6 +467,31 @@ def run_zr(args, w):
     if not args.no_chain and w.A == 1:
         overlap = measure_overlap(torch, zr, plan, grads, state, hyper, dev, stream)
 
+    offload = None
+    if not args.no_chain and w.A == 1 and ws == 1:
+        # ZeRO-Offload: reduce-scatter on the GPU, AdamW on the host cores over host-resident fp32 state,
+        # 4 B/param of sums down and 2 B/param of parameters back over the host link
+        nthreads = os.cpu_count() or 8
+        sums_dev = torch.empty(n, dtype=torch.float32, device=dev)
+        sums_host = torch.empty(n, dtype=torch.float32, pin_memory=True)
+        param_host = torch.empty(n, dtype=plan.torch_dtype(), pin_memory=True)
+        h_master = np.full(n, 0.01, np.float32)
+        h_m = np.zeros(n, np.float32)
+        h_v = np.zeros(n, np.float32)
+        plan.offload_step(grads, sums_dev, sums_host, h_master, h_m, h_v, param_host, state.param[0], hyper,
+                          w.init_scale, 1, nthreads, stream=stream)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for i in range(2):
+            plan.offload_step(grads, sums_dev, sums_host, h_master, h_m, h_v, param_host, state.param[0], hyper,
+                              w.init_scale, 2 + i, nthreads, stream=stream)
+        torch.cuda.synchronize(dev)
+        o_ms = (time.perf_counter() - t0) / 2 * 1e3
+        offload = {"ms_per_step": o_ms, "Gparams_per_s": plan.n_real / o_ms / 1e6, "host_threads": nthreads,
+                   "link_bytes_per_param": 6, "host_state_GB": 12 * n / 1e9,
+                   "call": "zr_offload_step (reduce-scatter on GPU, AdamW on the host CPU, params back)"}
+        del sums_dev, sums_host, param_host, h_master, h_m, h_v
+
     e2e = None
     cpu = None
     if not args.no_e2e:
@@ -509,6 +534,7 @@ def run_zr(args, w):
         "unfused_chain": chain,
         "zero3_param_gather": zero3,
         "bucketed_overlap": overlap,
+        "zero_offload": offload,
         "gpu_launches": args.steps,
         "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
                    "reasons": clocks.get("reasons"), "samples": clocks.get("samples"),

@@ -307,6 +307,39 @@ zr_status zr_gather_params(zr_plan* p, int bucket_lo, int bucket_hi, const void*
                            void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* ZeRO-Offload: the optimizer on the host CPU                                */
+/* ------------------------------------------------------------------------- */
+
+/* The owner-side update of zr_adamw_shard_step followed by the cast of zr_all_gather,
+ * run on the host CPU over host memory ([P2] (16) ZeRO-Offload: the update, which
+ * needs little compute, and the optimizer states move to the CPU, forward and
+ * backward stay on the GPU; [P2] 总结: offloaded to the CPU side). Same arithmetic and
+ * op order, so the same bits. sums, master, m, v: host fp32[n]; param16: host, n
+ * values of dt (may be NULL to skip the cast); nthreads worker threads (1..256).
+ * If any sums value is not finite, *overflow = 1 and nothing is written; otherwise
+ * *overflow = 0. Errors: ZR_ERR_INVALID for bad sizes, null pointers, dt, t < 1,
+ * W < 1, a bad loss_scale. */
+zr_status zr_offload_adamw(const float* sums, float* master, float* m, float* v, void* param16, zr_dtype dt,
+                           int64_t n, const zr_adamw_hyper* h, float loss_scale, int W, int64_t t, int nthreads,
+                           int32_t* overflow);
+
+/* One ZeRO-Offload step over a plan (A = 1; 16-bit or fp32 gradients): the ring
+ * reduce-scatter of every bucket on the GPU into sums_dev (device fp32, plan numel),
+ * the global overflow flag read back first (a skip writes nothing), then bucket by
+ * bucket: the sums copied into sums_host (pinned host fp32), the update on the CPU of
+ * the host-resident master/m/v (host fp32) into param_host (pinned host, plan dtype),
+ * and the parameters copied into param_dev (device replica). The host update of bucket
+ * b overlaps the copies of the other buckets. The last parameter copies are still
+ * queued on `stream` at return: synchronise it before reading param_dev or reusing
+ * param_host. The caller applies its loss-scale rule from *overflow (host int32).
+ * Errors: ZR_ERR_INVALID for null or misaligned buffers, stage, t < 1;
+ * ZR_ERR_UNSUPPORTED for A > 1; ZR_ERR_CUDA. */
+zr_status zr_offload_step(zr_plan* p, int stage, const void* const* grads, float* sums_dev, float* sums_host,
+                          float* master, float* m, float* v, void* param_host, void* param_dev,
+                          const zr_adamw_hyper* h, float loss_scale, int64_t t, int nthreads, void* stream,
+                          int32_t* overflow);
+
+/* ------------------------------------------------------------------------- */
 /* Fused step without device allocation                                        */
 /* ------------------------------------------------------------------------- */
 

@@ -1,0 +1,67 @@
+"""ZeRO-Offload step on the GPU machine: reduce-scatter on the GPU, AdamW on the host CPU over host-resident
+master/m/v, parameters back to the device. Checked against the oracle bit for bit, including a skip."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zero_gradient_reduction_gb300 as zr
+import zrgen
+from zrgen.layout import Layout
+from test_parity_gpu import OHYPER, u16
+
+pytestmark = pytest.mark.gpu
+F32 = np.float32
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+@pytest.mark.parametrize("W,dtype", [(2, zr.F16), (4, zr.BF16)])
+def test_offload_step_matches_oracle(W, dtype):
+    numels = [300_000, 999, 120_000, 64]
+    S = 1024.0 if dtype == zr.F16 else 1.0
+    plan = zr.Plan(numels, W=W, dtype=dtype, stage=2, cap=200_000, order=list(range(W))[::-1])
+    n = plan.numel
+    lay = Layout(numels, plan.tensor_offsets, np.full(len(numels), 1e-2, F32), 6, dtype)
+    table = torch.from_numpy(zrgen.normal_table().copy()).cuda()
+    cs = torch.cuda.current_stream().cuda_stream
+    tdt = plan.torch_dtype()
+    grads = [torch.zeros(n, dtype=tdt, device="cuda") for _ in range(W)]
+    sums_dev = torch.empty(n, dtype=torch.float32, device="cuda")
+    sums_host = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    master = lay.master_host(0, n)
+    m, v = np.zeros(n, F32), np.zeros(n, F32)
+    param_host = torch.empty(n, dtype=tdt, pin_memory=True)
+    param_dev = torch.zeros(n, dtype=tdt, device="cuda")
+    o = [master.copy(), m.copy(), v.copy(), np.zeros(n, np.uint16)]
+    osc = oracle.new_scaler(S, dynamic=True)
+    t = 0
+    for step in (1, 2, 3):
+        for r in range(W):
+            lay.grads_dev(grads[r], step, r, S, table, cs)
+        og = [lay.grads_host(0, n, step, r, S) for r in range(W)]
+        if step == 2:  # a non-finite gradient: the whole step is skipped
+            grads[1].view(torch.int16)[7] = 0x7C00 if dtype == zr.F16 else 0x7F80
+            og[1][7] = 0x7C00 if dtype == zr.F16 else 0x7F80
+        before = master.tobytes()
+        of = plan.offload_step(grads, sums_dev, sums_host, master, m, v, param_host, param_dev, zr.AdamW(), S,
+                               t + 1, nthreads=8)
+        torch.cuda.synchronize()
+        rep, _ = oracle.step(W, 1, dtype, plan.buckets, og, *o, OHYPER, osc, order=list(range(W))[::-1])
+        assert of == rep.overflow == (1 if step == 2 else 0)
+        if of:
+            assert master.tobytes() == before
+            S = osc.scale
+            continue
+        t += 1
+        for a, b in zip((master, m, v), o[:3]):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+        assert np.array_equal(u16(param_dev), o[3])
+    plan.close()

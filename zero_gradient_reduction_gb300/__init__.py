@@ -92,6 +92,10 @@ def lib():
                 "zr_all_gather": (st, [vp, i64, i32, vp, i32, vp]),
                 "zr_accumulate": (st, [vp, i32, vp, i64, i32, vp]),
                 "zr_step_bucket": (st, [vp, i32, i32, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp]),
+                "zr_offload_adamw": (st, [vp, vp, vp, vp, vp, i32, i64, ctypes.POINTER(Hyper), ctypes.c_float, i32,
+                                          i64, i32, ctypes.POINTER(ctypes.c_int32)]),
+                "zr_offload_step": (st, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(Hyper),
+                                         ctypes.c_float, i64, i32, vp, ctypes.POINTER(ctypes.c_int32)]),
                 "zr_plan_shard_numel": (i64, [vp, i32]),
                 "zr_plan_shard_offset": (st, [vp, i32, i32, ctypes.POINTER(ctypes.c_int64)]),
                 "zr_shard_params": (st, [vp, vp, vp, vp]),
@@ -222,6 +226,22 @@ def accumulate(grad, acc, first: bool, n: Optional[int] = None, stream=None) -> 
     _check(lib().zr_accumulate(_ptr(grad), _dt_of(grad), _ptr(acc), n, 1 if first else 0, _stream_handle(stream)))
 
 
+def _host_ptr(a) -> int:
+    return a.ctypes.data if isinstance(a, np.ndarray) else int(a.data_ptr())
+
+
+def offload_adamw(sums, master, m, v, param16, dtype: int, hyper: AdamW, loss_scale: float, W: int, t: int,
+                  nthreads: int = 8) -> int:
+    """ZeRO-Offload's host update (zr_offload_adamw) on host arrays (numpy or CPU tensors); returns the flag."""
+    n = int(sums.size if isinstance(sums, np.ndarray) else sums.numel())
+    h = hyper.c()
+    of = ctypes.c_int32(0)
+    _check(lib().zr_offload_adamw(_host_ptr(sums), _host_ptr(master), _host_ptr(m), _host_ptr(v),
+                                  _host_ptr(param16) if param16 is not None else None, int(dtype), n, ctypes.byref(h),
+                                  float(loss_scale), int(W), int(t), int(nthreads), ctypes.byref(of)))
+    return int(of.value)
+
+
 def all_gather(master, replicas: Sequence, n: Optional[int] = None, stream=None) -> None:
     n = int(master.numel()) if n is None else int(n)
     arr = _ptr_array(replicas)
@@ -341,6 +361,20 @@ class Plan:
         for b, ev in enumerate(ready_events):
             side_stream.wait_event(ev)
             self.step_bucket(b, grads, state, hyper, stage=stage, stream=side_stream)
+
+    def offload_step(self, grads: Sequence, sums_dev, sums_host, master, m, v, param_host, param_dev, hyper: AdamW,
+                     loss_scale: float, t: int, nthreads: int = 8, stage: Optional[int] = None, stream=None) -> int:
+        """ZeRO-Offload step (zr_offload_step): reduce-scatter on the GPU, AdamW on the host CPU over the host
+        master/m/v, parameters copied back. Returns the overflow flag; the last copies are still queued."""
+        arr = _ptr_array(grads)
+        h = hyper.c()
+        of = ctypes.c_int32(0)
+        _check(lib().zr_offload_step(self._h, int(stage if stage is not None else self.stage), ctypes.addressof(arr),
+                                     _ptr(sums_dev), _host_ptr(sums_host), _host_ptr(master), _host_ptr(m),
+                                     _host_ptr(v), _host_ptr(param_host), _ptr(param_dev), ctypes.byref(h),
+                                     float(loss_scale), int(t), int(nthreads), _stream_handle(stream),
+                                     ctypes.byref(of)))
+        return int(of.value)
 
     def step_from_host(self, host_grads: Sequence, dev_grads: Sequence, state: State, hyper: AdamW,
                        stage: Optional[int] = None, stream=None) -> StepReport:

@@ -19,8 +19,10 @@ OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libzr.so")
 ARCH = os.environ.get("ZR_CUDA_ARCH", "103a")
 
-CU = ["zr_step.cu", "zr_collectives.cu", "zr_noalloc.cu", "zr_zero3.cu"]
-CPP = ["zr_host.cpp"]
+CU = ["zr_step.cu", "zr_collectives.cu", "zr_noalloc.cu", "zr_zero3.cu", "zr_offload.cu"]
+CPP = ["zr_host.cpp", "zr_offload_host.cpp"]
+# the host AdamW of ZeRO-Offload: vectorised (no errno on sqrt), still one rounding per op
+CPP_EXTRA = {"zr_offload_host.cpp": ["-O3", "-fno-math-errno", "-pthread"]}
 HEADERS = [os.path.join(INCLUDE, "zr.h"), os.path.join(CSRC, "zr_internal.h"), os.path.join(CSRC, "zr_device.cuh"),
            os.path.join(CSRC, "zr_step_kernel.cuh"), os.path.join(CSRC, "zr_plan.h")]
 
@@ -49,7 +51,7 @@ def _compile(src: str, verbose_ptxas: bool):
         cmd = ["nvcc", "-c", path, "-o", obj] + _nvcc_flags(verbose_ptxas)
     else:
         cmd = ["g++", "-c", path, "-o", obj, "-O2", "-std=c++17", "-fPIC", "-ffp-contract=off", f"-I{INCLUDE}",
-               f"-I{CSRC}"]
+               f"-I{CSRC}"] + CPP_EXTRA.get(src, [])
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"compile failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
@@ -73,7 +75,8 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
                 sys.stdout.write(f"--- {s}\n{log}")
     if force or _stale(LIB, objs):
         tmp = LIB + f".{os.getpid()}.tmp"
-        cmd = ["nvcc", "-shared", "-cudart", "shared", f"-gencode=arch=compute_{ARCH},code=sm_{ARCH}", "-o", tmp] + objs
+        cmd = ["nvcc", "-shared", "-cudart", "shared", f"-gencode=arch=compute_{ARCH},code=sm_{ARCH}", "-o", tmp] + \
+            objs + ["-lpthread"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

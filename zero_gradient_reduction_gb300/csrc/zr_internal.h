@@ -28,6 +28,8 @@ struct Ctrl {
   int32_t stage;          // stage of the last step
   int64_t good, t, steps, skipped;
   double prod1, prod2;    // beta1^t, beta2^t (running products)
+  int32_t offload_flag;   // overflow flag of the reduce-scatter in zr_offload_step
+  int32_t pad;
 };
 
 }  // namespace zr

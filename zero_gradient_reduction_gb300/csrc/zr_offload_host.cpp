@@ -1,0 +1,141 @@
+// ZeRO-Offload's optimizer half on the host CPU: the owner-side AdamW update of fp32
+// master/m/v kept in host memory and the 16-bit cast of the result, run by a team of
+// threads over contiguous slices. Same arithmetic and op order as the GPU kernels
+// (each fp32 operation rounded once; built with -ffp-contract=off), so the result is
+// bit-identical to zr_adamw_shard_step + zr_all_gather.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "zr_internal.h"
+
+using zr::fail;
+
+namespace {
+
+uint32_t f32_bits(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  return u;
+}
+
+// Round-to-nearest-even fp32 -> bfloat16 / binary16 bit patterns.
+uint16_t to_bf16(float f) {
+  uint32_t x = f32_bits(f);
+  if ((x & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)(((x >> 16) & 0x8000u) | 0x7FC0u);
+  x += 0x7FFFu + ((x >> 16) & 1u);
+  return (uint16_t)(x >> 16);
+}
+
+uint16_t to_f16(float f) {
+  const uint32_t x = f32_bits(f);
+  const uint32_t sign = (x >> 16) & 0x8000u, a = x & 0x7FFFFFFFu;
+  if (a > 0x7F800000u) return (uint16_t)(sign | 0x7E00u);
+  if (a >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);  // rounds to infinity
+  if (a < 0x38800000u) {                                      // subnormal result or zero
+    if (a < 0x33000000u) return (uint16_t)sign;
+    const uint32_t mant = (a & 0x7FFFFFu) | 0x800000u, shift = 126u - (a >> 23);
+    uint32_t r = mant >> shift;
+    const uint32_t rem = mant & ((1u << shift) - 1u), half = 1u << (shift - 1u);
+    if (rem > half || (rem == half && (r & 1u))) ++r;
+    return (uint16_t)(sign | r);
+  }
+  uint32_t r = (a - 0x38000000u) >> 13;
+  const uint32_t rem = a & 0x1FFFu;
+  if (rem > 0x1000u || (rem == 0x1000u && (r & 1u))) ++r;
+  return (uint16_t)(sign | r);
+}
+
+struct Consts {
+  float b1, b2, omb1, omb2, lr, eps, decay, bc1, bc2, r;
+};
+
+void update_slice(const float* __restrict__ sums, float* __restrict__ p, float* __restrict__ m,
+                  float* __restrict__ v, uint16_t* __restrict__ out, int64_t lo, int64_t hi, const Consts k, bool bf16) {
+  for (int64_t i = lo; i < hi; ++i) {
+    const float g = sums[i] * k.r;
+    const float mi = k.b1 * m[i] + k.omb1 * g;
+    const float vi = k.b2 * v[i] + k.omb2 * (g * g);
+    const float mhat = mi / k.bc1;
+    const float vhat = vi / k.bc2;
+    const float den = std::sqrt(vhat) + k.eps;
+    const float u = mhat / den;
+    const float pi = p[i] * k.decay - k.lr * u;
+    m[i] = mi;
+    v[i] = vi;
+    p[i] = pi;
+  }
+  if (out) {
+    if (bf16)
+      for (int64_t i = lo; i < hi; ++i) out[i] = to_bf16(p[i]);
+    else
+      for (int64_t i = lo; i < hi; ++i) out[i] = to_f16(p[i]);
+  }
+}
+
+bool any_nonfinite(const float* x, int64_t lo, int64_t hi) {
+  bool bad = false;
+  for (int64_t i = lo; i < hi; ++i) bad |= ((f32_bits(x[i]) & 0x7F800000u) == 0x7F800000u);
+  return bad;
+}
+
+template <typename F>
+void parallel_for(int64_t n, int nthreads, F fn) {
+  if (nthreads <= 1 || n < (1 << 16)) {
+    fn(0, n, 0);
+    return;
+  }
+  std::vector<std::thread> team;
+  const int64_t per = (n + nthreads - 1) / nthreads;
+  for (int t = 0; t < nthreads; ++t) {
+    const int64_t lo = t * per, hi = lo + per < n ? lo + per : n;
+    if (lo >= hi) break;
+    team.emplace_back(fn, lo, hi, t);
+  }
+  for (auto& th : team) th.join();
+}
+
+}  // namespace
+
+namespace zr {
+float bias_correction_host(float beta, int64_t t);
+}
+
+extern "C" zr_status zr_offload_adamw(const float* sums, float* master, float* m, float* v, void* param16,
+                                      zr_dtype dt, int64_t n, const zr_adamw_hyper* h, float loss_scale, int W,
+                                      int64_t t, int nthreads, int32_t* overflow) {
+  zr::clear_error();
+  if (n < 0 || W < 1 || t < 1 || !h || !overflow) return fail(ZR_ERR_INVALID, "zr_offload_adamw: bad n/W/t or null");
+  if (dt != ZR_F16 && dt != ZR_BF16) return fail(ZR_ERR_INVALID, "zr_offload_adamw: dtype must be F16 or BF16");
+  if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale))
+    return fail(ZR_ERR_INVALID, "zr_offload_adamw: loss_scale must be positive and finite");
+  if (n > 0 && (!sums || !master || !m || !v)) return fail(ZR_ERR_INVALID, "zr_offload_adamw: null array");
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  std::vector<char> bad(nthreads, 0);
+  parallel_for(n, nthreads, [&](int64_t lo, int64_t hi, int tid) { bad[tid] = any_nonfinite(sums, lo, hi); });
+  for (char b : bad)
+    if (b) {
+      *overflow = 1;
+      return ZR_OK;  // skipped: nothing written
+    }
+  *overflow = 0;
+  Consts k;
+  k.b1 = h->beta1;
+  k.b2 = h->beta2;
+  k.omb1 = 1.0f - h->beta1;
+  k.omb2 = 1.0f - h->beta2;
+  k.lr = h->lr;
+  k.eps = h->eps;
+  const float lrwd = h->lr * h->weight_decay;
+  k.decay = 1.0f - lrwd;
+  k.bc1 = zr::bias_correction_host(h->beta1, t);
+  k.bc2 = zr::bias_correction_host(h->beta2, t);
+  k.r = (float)(1.0 / ((double)loss_scale * (double)W));
+  uint16_t* out = static_cast<uint16_t*>(param16);
+  const bool bf16 = dt == ZR_BF16;
+  parallel_for(n, nthreads, [&](int64_t lo, int64_t hi, int) { update_slice(sums, master, m, v, out, lo, hi, k, bf16); });
+  return ZR_OK;
+}
