@@ -118,3 +118,21 @@ def test_overlapped_schedule_matches_oracle():
         L = sa.live(rep.current)
         assert_state_close(L["master"].cpu().numpy(), L["m"].cpu().numpy(), L["v"].cpu().numpy(),
                            u16(L["param"]), *o, exact=True, where=f"overlapped step {step}: ")
+
+
+def test_graph_replay_steps_like_direct_calls():
+    """A CUDA graph of one zr_step, replayed, keeps stepping (live set, scale and t come from device memory)
+    and gives the same bytes as calling zr_step each time."""
+    plans, lay, table, (sa, sb) = _setup(W=2, dtype=zr.BF16, S=1.0)
+    n = plans[0].numel
+    grads = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    for r in range(2):
+        lay.grads_dev(grads[r], 1, r, 1.0, table, torch.cuda.current_stream().cuda_stream)
+    g = plans[1].capture(grads, sb, HYPER)
+    for _ in range(3):
+        plans[0].step(grads, sa, HYPER)
+        g.replay()
+    torch.cuda.synchronize()
+    ra, rb = plans[0].report(), plans[1].report()
+    assert ra.t == rb.t == 3 and ra.current == rb.current
+    assert _live_bytes(sa, ra.current) == _live_bytes(sb, rb.current)

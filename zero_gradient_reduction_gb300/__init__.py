@@ -344,6 +344,20 @@ class Plan:
                              ctypes.byref(rep) if rep is not None else None))
         return rep
 
+    def capture(self, grads: Sequence, state: State, hyper: AdamW, stage: Optional[int] = None, steps: int = 1):
+        """A CUDA graph of `steps` fused steps on these buffers (torch.cuda.CUDAGraph; replay() runs them).
+        The step reads its live set, loss scale and t from device memory at run time, so replays keep
+        stepping correctly; the graph keeps the buffer addresses it was captured with."""
+        import torch
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(steps):
+                self.step(grads, state, hyper, stage=stage, stream=side)
+        torch.cuda.current_stream().wait_stream(side)
+        return g
+
     def step_bucket(self, bucket: int, grads: Sequence, state: State, hyper: AdamW, stage: Optional[int] = None,
                     stream=None) -> None:
         """One bucket of a step (zr_step_bucket): call for buckets 0..nb-1 in order; the last commits."""

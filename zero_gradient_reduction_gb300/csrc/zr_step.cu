@@ -103,7 +103,22 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   for (int t = 0; t < d->ntensors; ++t) p->n_real += d->numels[t];
   p->numel = nb ? p->buckets.back().start + p->buckets.back().len : 0;
 
-  // Tile schedule: every block of every bucket cut into pieces of at most kTileElems.
+  // Kernel for (dtype, W, A) and the number of blocks that fit on the GPU at once.
+  const bool f32 = p->fp32_grads != 0;
+  KernelFn k = p->dtype == ZR_F16 ? pick_kernel<zr::DT_F16>(p->W, p->A, f32) : pick_kernel<zr::DT_BF16>(p->W, p->A, f32);
+  p->kernel = reinterpret_cast<void*>(k);
+  int per_sm = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&p->device);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, 0);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+  if (per_sm < 1) per_sm = 1;
+  const int64_t full = (int64_t)(sms > 0 ? sms : 1) * per_sm;
+
+  // Tile schedule: every block of every bucket cut into pieces of at most `tile` elements.
+  // Large plans use kTileElems; a small plan halves the tile (down to 2048 elements)
+  // until it has at least two tiles for every resident block, so that it fills the GPU.
+  int64_t tile = kTileElems;
+  while (tile > 2048 && p->numel / tile < 2 * full) tile /= 2;
   std::vector<int4> tiles;
   for (const zr_bucket& b : p->buckets) {
     p->tile_begin.push_back((int64_t)tiles.size());
@@ -112,15 +127,20 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
       const int64_t end = b.start + b.len;
       if (lo > end) lo = end;
       if (hi > end) hi = end;
-      for (int64_t x = lo; x < hi; x += kTileElems) {
-        const int64_t len = (hi - x) < kTileElems ? (hi - x) : kTileElems;
+      for (int64_t x = lo; x < hi; x += tile) {
+        const int64_t len = (hi - x) < tile ? (hi - x) : tile;
         tiles.push_back(make_int4((int)(uint32_t)(uint64_t)x, (int)(uint32_t)((uint64_t)x >> 32), (int)(len / 8), c));
       }
     }
   }
   p->ntiles = (int64_t)tiles.size();
   p->tile_begin.push_back(p->ntiles);
-  cudaError_t e = cudaGetDevice(&p->device);
+  p->grid = (int)(p->ntiles < full ? (p->ntiles > 0 ? p->ntiles : 1) : full);
+  for (size_t b = 0; b + 1 < p->tile_begin.size(); ++b) {
+    const int64_t nt = p->tile_begin[b + 1] - p->tile_begin[b];
+    p->bucket_grid.push_back((int)(nt < full ? nt : full));
+    p->bucket_blocks += (unsigned)p->bucket_grid.back();
+  }
   if (e == cudaSuccess && !tiles.empty()) e = cudaMalloc(&p->tiles_dev, tiles.size() * sizeof(int4));
   if (e == cudaSuccess && !tiles.empty())
     e = cudaMemcpy(p->tiles_dev, tiles.data(), tiles.size() * sizeof(int4), cudaMemcpyHostToDevice);
@@ -128,24 +148,6 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   if (e == cudaSuccess) {
     zr::Ctrl c = initial_ctrl(p->scaler);
     e = cudaMemcpy(p->ctrl_dev, &c, sizeof c, cudaMemcpyHostToDevice);
-  }
-  if (e == cudaSuccess) {
-    const bool f32 = p->fp32_grads != 0;
-    KernelFn k = p->dtype == ZR_F16 ? pick_kernel<zr::DT_F16>(p->W, p->A, f32) : pick_kernel<zr::DT_BF16>(p->W, p->A, f32);
-    p->kernel = reinterpret_cast<void*>(k);
-    int per_sm = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, 0);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
-    if (e == cudaSuccess) {
-      if (per_sm < 1) per_sm = 1;
-      const int64_t full = (int64_t)sms * per_sm;
-      p->grid = (int)(p->ntiles < full ? (p->ntiles > 0 ? p->ntiles : 1) : full);
-      for (size_t b = 0; b + 1 < p->tile_begin.size(); ++b) {
-        const int64_t nt = p->tile_begin[b + 1] - p->tile_begin[b];
-        p->bucket_grid.push_back((int)(nt < full ? nt : full));
-        p->bucket_blocks += (unsigned)p->bucket_grid.back();
-      }
-    }
   }
   if (e != cudaSuccess) {
     zr_status s = cuda_fail("zr_plan_create", e);
