@@ -376,6 +376,36 @@ def run_zr(args, w):
     achieved = rep.bytes_alg / (ms_total / args.steps * 1e-3) / 1e9
     traffic, _digest = _traffic_record(w.name)
 
+    # the in-place step (zr_step_inplace: a flag pass, then AdamW in place on ONE state set, for runs with
+    # no room for a second set), timed right after the step it is compared with, on the live set of the
+    # ping-pong state so that it needs no memory of its own: (4*W*A + 26) bytes per param, two launches
+    inplace = None
+    if not args.no_chain:
+        k = plan.report(stream).current
+        one = zr.State1.of(state.master[k], state.m[k], state.v[k], state.param[k])
+        for _ in range(3):
+            plan.step_inplace(grads, one, hyper, stream=stream)
+        torch.cuda.synchronize(dev)
+        g_ip = plan.capture(grads, one, hyper)
+        torch.cuda.synchronize(dev)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(args.chain_steps):
+            g_ip.replay()
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        ip_rep = plan.report(stream)
+        assert ip_rep.overflow == 0 and ip_rep.current == k, ip_rep.as_dict()
+        ip_ms = c0.elapsed_time(c1) / args.chain_steps
+        ip_bpp = 4 * w.W * w.A + 26
+        inplace = {"ms_per_step": ip_ms, "Gparams_per_s": plan.n_real / ip_ms / 1e6, "alg_bytes_per_param": ip_bpp,
+                   "hbm_GBs": ip_bpp * plan.n_real / ip_ms / 1e6,
+                   "frac_of_measured_copy": ip_bpp * plan.n_real / ip_ms / 1e6 / peak,
+                   "launches_per_step": 2, "state_bytes_saved_GB": 14 * n / 1e9,
+                   "call": "zr_step_inplace captured as a CUDA graph (flag pass, then the update in place)"}
+        del g_ip, one
+
     # comparison point: the same step as the unfused chain of standalone calls (reduce-scatter per bucket
     # into fp32 sums, flag pass + AdamW in place, cast/all-gather), (2W + 38) bytes per param
     chain = None
@@ -542,6 +572,7 @@ def run_zr(args, w):
         "e2e": e2e,
         "unfused_chain": chain,
         "zero3_param_gather": zero3,
+        "inplace_step": inplace,
         "bucketed_overlap": overlap,
         "zero_offload": offload,
         "gpu_launches": args.steps,

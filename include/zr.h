@@ -198,7 +198,8 @@ typedef struct {
     int64_t skipped_total;
     int64_t good;          /* clean steps since the last scale change */
     int64_t n_real;        /* parameters (sum of numels) */
-    int64_t bytes_alg;     /* algorithmic HBM bytes of one step: (2*W*A + 26) * n_real */
+    int64_t bytes_alg;     /* algorithmic HBM bytes of one zr_step: (2*W*A + 26) * n_real
+                              (16-bit gradients; zr_step_inplace adds 2*W*A * n_real) */
 } zr_step_report;
 
 /* Builds the bucket table, the tile schedule and the device control block.
@@ -253,6 +254,38 @@ zr_status zr_step_from_host(zr_plan* p, int stage, const void* const* host_grads
  * for a bucket index outside [0, nbuckets). */
 zr_status zr_step_bucket(zr_plan* p, int stage, int bucket, const void* const* grads, const zr_state* st,
                          const zr_adamw_hyper* h, void* stream);
+
+/* The optimizer state and the parameter replica as ONE set (zr_step_inplace). Device
+ * pointers, zr_plan_numel elements each; param is of the plan's dtype. */
+typedef struct {
+    float* master;
+    float* m;
+    float* v;
+    void* param;
+} zr_state1;
+
+/* The fused step on one state set, updated in place, for runs whose HBM has no room for
+ * zr_state's second set: it saves 14 bytes per parameter (12 of fp32 master/m/v, 2 of the
+ * 16-bit replica), e.g. 98 GB for a 7B-parameter model. Same arithmetic, overflow rule
+ * and loss-scale rule as zr_step ([P1] 三 ZeRO-1; [P2] 核心技术 (3) dynamic scaling).
+ * The skip decision covers the whole step and must be known before any state is
+ * overwritten, so the call makes two launches on `stream`:
+ *   1. a flag pass over every bucket: the same ring-order fp32 sums as the update, kept
+ *      only for their non-finite flag (reads 2*W*A bytes per parameter; 4*W*A for fp32
+ *      gradients);
+ *   2. the update: if the flag is set nothing is written, so the set stays bit-unchanged;
+ *      otherwise master/m/v/param are read and rewritten in place. Its last block applies
+ *      the loss-scale rule and counts the step.
+ * Algorithmic bytes per parameter: 4*W*A + 26 for 16-bit gradients. The control block's
+ * current index is neither used nor changed (after ping-pong steps on the same plan,
+ * pass the live set). Both launches can be captured in a CUDA graph. There is no
+ * bucket-by-bucket form (zr_step_bucket): no bucket may be updated before the flag of
+ * the last one is known.
+ * rep: NULL for an asynchronous call, else the call synchronises `stream` and fills it.
+ * Errors: ZR_ERR_INVALID for a null plan/state/hyper/grads, stage outside 1..3, a null or
+ * misaligned array; ZR_ERR_CUDA. */
+zr_status zr_step_inplace(zr_plan* p, int stage, const void* const* grads, const zr_state1* st,
+                          const zr_adamw_hyper* h, void* stream, zr_step_report* rep);
 
 /* Synchronises `stream` and reads the control block into *rep. */
 zr_status zr_plan_report(zr_plan* p, void* stream, zr_step_report* rep);

@@ -115,3 +115,6 @@ def test_argument_checks_without_gpu(zr):
     out = ctypes.c_void_p()
     assert L.zr_plan_create(ctypes.byref(d), ctypes.byref(out)) == 1  # stage 0
     assert L.zr_model_state_bytes(9, 10, 1) == -1
+    s1 = zr.StateC1(16, 16, 16, 16)
+    assert L.zr_step_inplace(None, 2, ctypes.addressof(one), ctypes.byref(s1), ctypes.byref(h), None, None) == 1
+    assert b"zr_step_inplace" in L.zr_last_error()

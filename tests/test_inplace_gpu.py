@@ -1,0 +1,145 @@
+"""The in-place step (zr_step_inplace): one state set, a flag pass before the update.
+
+It must give the oracle's bits, the same bits as the ping-pong step on the same inputs, and on an
+overflow step it must leave the single set bit-unchanged (the skip of page "并行训练框架DeepSpeed介绍",
+核心技术 (3), taken before anything is overwritten)."""
+import numpy as np
+import pytest
+import torch
+
+import zero_gradient_reduction_gb300 as zr
+from test_parity_gpu import HYPER, FusedRun
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.empty_cache()
+
+
+class InPlaceRun(FusedRun):
+    """FusedRun on a single state set, stepped with zr_step_inplace."""
+
+    def __init__(self, *args, **kw):
+        super().__init__(*args, **kw)
+        s1 = self.plan.new_state1()
+        s1.master.copy_(self.state.master[0])
+        s1.param.copy_(self.state.param[0])
+        self.state1 = s1
+        self.state = None  # the ping-pong sets are not used
+
+    def _launch(self, stage):
+        rep = self.plan.step_inplace(self.grads, self.state1, HYPER, stage=stage, report=True)
+        assert rep.current == 0
+        return rep
+
+    def live(self):
+        s = self.state1
+        return (s.master.cpu().numpy(), s.m.cpu().numpy(), s.v.cpu().numpy(),
+                s.param.cpu().view(torch.int16).numpy().view(np.uint16))
+
+
+@pytest.mark.parametrize("W,A,dtype", [(1, 1, zr.BF16), (2, 1, zr.F16), (3, 1, zr.BF16), (5, 1, zr.F16),
+                                       (8, 1, zr.BF16), (2, 4, zr.BF16), (4, 4, zr.F16), (3, 3, zr.BF16),
+                                       (16, 1, zr.F16)])
+def test_inplace_ragged_buckets_bit_exact(W, A, dtype):
+    rng = np.random.default_rng(W * 100 + A + 7)
+    numels = [1000, 37, 5000, 8, 123_457, 64, 9_999, 3, 40_000]
+    order = list(rng.permutation(W))
+    run = InPlaceRun(numels, W, A, dtype, cap=20_000, S=8.0, order=order, seed=4,
+                     sigma=rng.uniform(1e-3, 1e-1, size=len(numels)))
+    assert len(run.plan.buckets) >= 4
+    for s in range(1, 4):
+        rep, _ = run.step(s)
+        assert rep.t == s
+        run.check(f"in place W={W} A={A} step {s}: ")
+
+
+def test_inplace_equals_pingpong_with_a_skip():
+    """Same seeded inputs through both modes, an overflow at step 2: identical bytes after every step."""
+    numels = [60_000, 333, 20_001]
+    kw = dict(cap=30_000, S=65536.0, dynamic=True, seed=6, interval=2)
+    pp = FusedRun(numels, 4, 1, zr.F16, **kw)
+    ip = InPlaceRun(numels, 4, 1, zr.F16, **kw)
+    inj = (2, int(pp.plan.tensor_offsets[2]) + 5)
+    for s in range(1, 6):
+        rp, _ = pp.step(s, inject=inj if s == 2 else None)
+        ri, _ = ip.step(s, inject=inj if s == 2 else None)
+        for f in ("overflow", "skipped", "t", "steps", "skipped_total", "good"):
+            assert getattr(rp, f) == getattr(ri, f), f
+        assert rp.scale_used == ri.scale_used and rp.scale == ri.scale
+        for x, y in zip(pp.live(), ip.live()):
+            assert x.tobytes() == y.tobytes(), f"step {s}"
+
+
+@pytest.mark.parametrize("dtype", [zr.F16, zr.BF16])
+def test_inplace_skip_leaves_the_set_unchanged(dtype):
+    numels = [20_000, 4_000, 30_000]
+    run = InPlaceRun(numels, 2, 1, dtype, cap=25_000, S=65536.0, dynamic=True, seed=5)
+    run.step(1)
+    before = [x.copy() for x in run.live()]
+    rep, _ = run.step(2, inject=(1, int(run.plan.tensor_offsets[1]) + 99))
+    assert rep.overflow == 1 and rep.skipped == 1 and rep.t == 1 and rep.scale == 32768.0
+    for a, b in zip(run.live(), before):
+        assert a.tobytes() == b.tobytes()
+    for s in (3, 4):
+        rep, _ = run.step(s)
+        assert rep.overflow == 0
+        run.check(f"resume step {s}: ")
+    assert rep.t == 3 and rep.skipped_total == 1
+
+
+def test_inplace_scale_growth():
+    run = InPlaceRun([4096, 1000], 2, 1, zr.BF16, cap=10_000, S=4.0, dynamic=True, interval=2)
+    scales = [run.step(s)[0].scale_used for s in range(1, 6)]
+    assert scales == [4.0, 4.0, 8.0, 8.0, 16.0]
+    run.check()
+
+
+def test_inplace_graph_replay_equals_eager():
+    """Both launches of an in-place step captured in a CUDA graph; replays keep stepping (the flag and the
+    scaler live in device memory)."""
+    numels = [50_000, 1234]
+    a = InPlaceRun(numels, 3, 1, zr.BF16, cap=40_000, S=2.0, seed=8)
+    b = InPlaceRun(numels, 3, 1, zr.BF16, cap=40_000, S=2.0, seed=8)
+    st = torch.cuda.current_stream().cuda_stream
+    for r in range(3):  # one fixed set of gradients, stepped three times
+        a.layout.grads_dev(a.grads[r], 1, r, 2.0, a.table, st)
+        b.layout.grads_dev(b.grads[r], 1, r, 2.0, b.table, st)
+    for _ in range(3):
+        a.plan.step_inplace(a.grads, a.state1, HYPER)
+    g = b.plan.capture(b.grads, b.state1, HYPER, steps=1)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ra, rb = a.plan.report(), b.plan.report()
+    assert ra.t == rb.t == 3 and ra.current == rb.current == 0
+    for x, y in zip(a.live(), b.live()):
+        assert x.tobytes() == y.tobytes()
+
+
+def test_inplace_error_paths():
+    plan = zr.Plan([1024], W=2, A=1, dtype=zr.BF16, stage=2, cap=2048)
+    s1 = plan.new_state1()
+    grads = [torch.zeros(plan.numel, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    with pytest.raises(zr.ZrError) as e:
+        plan.step_inplace(grads, s1, HYPER, stage=0)
+    assert e.value.status == 1
+    with pytest.raises(zr.ZrError):
+        plan.step_inplace([grads[0], grads[1][1:]], s1, HYPER)  # 2-byte offset: misaligned
+    master = s1.master
+    s1.master = master[1:]  # 4-byte offset: misaligned
+    with pytest.raises(zr.ZrError):
+        plan.step_inplace(grads, s1, HYPER)
+    s1.master = master
+    # nothing above launched, and the control block is untouched
+    s1.master.zero_()
+    r = plan.step_inplace(grads, s1, HYPER, report=True)
+    assert r.t == 1 and r.steps == 1 and r.overflow == 0

@@ -31,7 +31,9 @@ def _gpu():
     torch.cuda.empty_cache()
 
 
-def run_sampled(w: zrgen.Workload, steps=None, extra_buckets=3):
+def run_sampled(w: zrgen.Workload, steps=None, extra_buckets=3, inplace=False):
+    """Steps the workload and checks sampled windows against the oracle; inplace: one state set,
+    stepped with zr_step_inplace."""
     steps = steps or w.steps
     plan = zr.Plan(list(w.tensors), W=w.W, A=w.A, dtype=w.dtype, stage=w.stage, cap=w.cap,
                    scaler=zr.Scaler(w.init_scale, w.dynamic))
@@ -39,10 +41,11 @@ def run_sampled(w: zrgen.Workload, steps=None, extra_buckets=3):
     cs = torch.cuda.current_stream().cuda_stream
     table = torch.from_numpy(zrgen.normal_table().copy()).cuda()
     n = plan.numel
-    state = plan.new_state()
-    state.master[0].zero_()
-    layout.master_dev(state.master[0], table, cs)
-    zr.all_gather(state.master[0], [state.param[0]])
+    state = plan.new_state1() if inplace else plan.new_state()
+    master0 = state.master if inplace else state.master[0]
+    master0.zero_()
+    layout.master_dev(master0, table, cs)
+    zr.all_gather(master0, [state.param if inplace else state.param[0]])
     grads = [torch.zeros(n, dtype=plan.torch_dtype(), device="cuda") for _ in range(w.W * w.A)]
 
     nb = len(plan.buckets)
@@ -70,7 +73,10 @@ def run_sampled(w: zrgen.Workload, steps=None, extra_buckets=3):
         if inj is not None:
             bits = 0x7C00 if w.dtype == zr.F16 else 0x7F80
             grads[inj[0]].view(torch.int16)[inj[1]] = int(np.uint16(bits).view(np.int16))
-        rep = plan.step(grads, state, HYPER, report=True)
+        if inplace:
+            rep = plan.step_inplace(grads, state, HYPER, report=True)
+        else:
+            rep = plan.step(grads, state, HYPER, report=True)
         want_flag = 1 if inj is not None else 0
         assert rep.overflow == want_flag and rep.skipped == want_flag, (s, rep.as_dict())
         oreps = ow.step(s, S, want_flag, inject=inj)
@@ -112,6 +118,22 @@ def test_7b_full_size_with_overflow_skip():
         pytest.skip(f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}")
     rep = run_sampled(w)
     # 6 steps, +inf at step 3: t = 5 committed updates, scale 65536 -> 32768, one skip
+    assert rep.t == 5 and rep.scale == 32768.0 and rep.skipped_total == 1 and rep.steps == 6
+
+
+def test_1p3b_full_size_in_place():
+    rep = run_sampled(zrgen.workload("1p3b"), inplace=True)
+    assert rep.t == 5 and rep.current == 0
+
+
+def test_7b_full_size_in_place_with_overflow_skip():
+    """One state set: 14 bytes per parameter less than the ping-pong sets (126 GB in all instead of 224)."""
+    w = zrgen.workload("7b")
+    free, _ = torch.cuda.mem_get_info()
+    need = w.n * (2 * w.W + 14) + (8 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}")
+    rep = run_sampled(w, inplace=True)
     assert rep.t == 5 and rep.scale == 32768.0 and rep.skipped_total == 1 and rep.steps == 6
 
 

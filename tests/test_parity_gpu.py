@@ -250,7 +250,7 @@ class FusedRun:
             bits = 0x7C00 if self.dtype == zr.F16 else 0x7F80
             self.grads[r].view(torch.int16)[i] = np.int16(np.uint16(bits).view(np.int16))
             ograds[r][i] = bits
-        rep = self.plan.step(self.grads, self.state, HYPER, stage=stage, report=True)
+        rep = self._launch(stage)
         orep, _ = oracle.step(self.W, self.A, self.dtype, self.plan.buckets, ograds, *self.o, OHYPER, self.osc,
                               order=self.order)
         assert rep.overflow == orep.overflow and rep.skipped == orep.skipped
@@ -259,6 +259,9 @@ class FusedRun:
         self.S = rep.scale
         self.current = rep.current
         return rep, orep
+
+    def _launch(self, stage):
+        return self.plan.step(self.grads, self.state, HYPER, stage=stage, report=True)
 
     def live(self):
         L = self.state.live(self.current)

@@ -54,6 +54,11 @@ class StateC(ctypes.Structure):
                 ("param", ctypes.c_void_p * 2)]
 
 
+class StateC1(ctypes.Structure):
+    _fields_ = [("master", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("param", ctypes.c_void_p)]
+
+
 class Checkpoint(ctypes.Structure):
     _fields_ = [("current", ctypes.c_int32), ("scale", ctypes.c_float), ("good", ctypes.c_int64),
                 ("t", ctypes.c_int64), ("steps", ctypes.c_int64), ("skipped", ctypes.c_int64),
@@ -108,6 +113,8 @@ def lib():
                 "zr_plan_reset": (st, [vp, vp]),
                 "zr_step": (st, [vp, i32, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp,
                                  ctypes.POINTER(StepReport)]),
+                "zr_step_inplace": (st, [vp, i32, vp, ctypes.POINTER(StateC1), ctypes.POINTER(Hyper), vp,
+                                         ctypes.POINTER(StepReport)]),
                 "zr_step_from_host": (st, [vp, i32, vp, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp,
                                            ctypes.POINTER(StepReport)]),
                 "zr_plan_report": (st, [vp, vp, ctypes.POINTER(StepReport)]),
@@ -287,6 +294,30 @@ class State:
         return dict(master=self.master[k], m=self.m[k], v=self.v[k], param=self.param[k])
 
 
+class State1:
+    """ONE set of fp32 master/m/v and the 16-bit parameter replica (the in-place step), as torch tensors."""
+
+    def __init__(self, numel: int, dtype, device="cuda"):
+        import torch
+        self.master = torch.empty(numel, dtype=torch.float32, device=device)
+        self.m = torch.zeros(numel, dtype=torch.float32, device=device)
+        self.v = torch.zeros(numel, dtype=torch.float32, device=device)
+        self.param = torch.empty(numel, dtype=dtype, device=device)
+
+    @classmethod
+    def of(cls, master, m, v, param) -> "State1":
+        """A State1 over existing tensors (e.g. one set of a State), with no allocation."""
+        s = cls.__new__(cls)
+        s.master, s.m, s.v, s.param = master, m, v, param
+        return s
+
+    def c(self) -> StateC1:
+        return StateC1(_ptr(self.master), _ptr(self.m), _ptr(self.v), _ptr(self.param))
+
+    def live(self, k: int = 0):
+        return dict(master=self.master, m=self.m, v=self.v, param=self.param)
+
+
 class Plan:
     """A bucketed ZeRO step over W emulated workers (zr_plan_create / zr_step)."""
 
@@ -344,17 +375,36 @@ class Plan:
                              ctypes.byref(rep) if rep is not None else None))
         return rep
 
-    def capture(self, grads: Sequence, state: State, hyper: AdamW, stage: Optional[int] = None, steps: int = 1):
-        """A CUDA graph of `steps` fused steps on these buffers (torch.cuda.CUDAGraph; replay() runs them).
-        The step reads its live set, loss scale and t from device memory at run time, so replays keep
-        stepping correctly; the graph keeps the buffer addresses it was captured with."""
+    def new_state1(self, device="cuda") -> State1:
+        return State1(self.numel, self.torch_dtype(), device)
+
+    def step_inplace(self, grads: Sequence, state: State1, hyper: AdamW, stage: Optional[int] = None, stream=None,
+                     report: bool = False):
+        """One step on a single state set, updated in place (zr_step_inplace): a flag pass, then the update."""
+        arr = _ptr_array(grads)
+        st = state.c()
+        h = hyper.c()
+        rep = StepReport() if report else None
+        _check(lib().zr_step_inplace(self._h, int(stage if stage is not None else self.stage), ctypes.addressof(arr),
+                                     ctypes.byref(st), ctypes.byref(h), _stream_handle(stream),
+                                     ctypes.byref(rep) if rep is not None else None))
+        return rep
+
+    def capture(self, grads: Sequence, state, hyper: AdamW, stage: Optional[int] = None, steps: int = 1):
+        """A CUDA graph of `steps` fused steps on these buffers (torch.cuda.CUDAGraph; replay() runs them):
+        ping-pong steps for a State, in-place steps for a State1. The step reads its live set, loss scale
+        and t from device memory at run time, so replays keep stepping correctly; the graph keeps the buffer
+        addresses it was captured with."""
         import torch
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.graph(g, stream=side):
             for _ in range(steps):
-                self.step(grads, state, hyper, stage=stage, stream=side)
+                if isinstance(state, State1):
+                    self.step_inplace(grads, state, hyper, stage=stage, stream=side)
+                else:
+                    self.step(grads, state, hyper, stage=stage, stream=side)
         torch.cuda.current_stream().wait_stream(side)
         return g
 

@@ -19,7 +19,7 @@ OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libzr.so")
 ARCH = os.environ.get("ZR_CUDA_ARCH", "103a")
 
-CU = ["zr_step.cu", "zr_collectives.cu", "zr_noalloc.cu", "zr_zero3.cu", "zr_offload.cu"]
+CU = ["zr_step.cu", "zr_inplace.cu", "zr_collectives.cu", "zr_noalloc.cu", "zr_zero3.cu", "zr_offload.cu"]
 CPP = ["zr_host.cpp", "zr_offload_host.cpp"]
 # the host AdamW of ZeRO-Offload: vectorised (no errno on sqrt), still one rounding per op
 CPP_EXTRA = {"zr_offload_host.cpp": ["-O3", "-fno-math-errno", "-pthread"]}

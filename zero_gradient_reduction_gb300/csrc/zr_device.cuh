@@ -34,6 +34,16 @@ __device__ __forceinline__ float4 ld_once_f4(const float* p) {
   return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
 }
 
+// As ld_once, on the coherent path: for data the same kernel later overwrites in place
+// (the non-coherent path is only defined for data that stays read-only for the launch).
+__device__ __forceinline__ float4 ld_rw_f4(const float* p) {
+  uint4 r;
+  asm("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return make_float4(__uint_as_float(r.x), __uint_as_float(r.y), __uint_as_float(r.z), __uint_as_float(r.w));
+}
+
 __device__ __forceinline__ void st_once_f4(float* p, float4 v) {
   st_once(p, make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w)));
 }

@@ -28,6 +28,11 @@ struct zr_plan {
   std::vector<int64_t> tile_begin;
   std::vector<int> bucket_grid;
   unsigned bucket_blocks = 0;
+  // in-place step (zr_step_inplace): the flag-pass and in-place instantiations for
+  // (dtype, W, A), each with the number of blocks that fit on the GPU at once
+  void* ip_flag_kernel = nullptr;
+  void* ip_update_kernel = nullptr;
+  int ip_flag_grid = 0, ip_update_grid = 0;
   // ZeRO-3 parameter shards: the worker at ring position p keeps block (p+1) mod W of
   // every bucket, packed in bucket order. shard_off[b*W + w] is where bucket b's block
   // starts in worker w's shard; the shard tile table cuts every (bucket, block) piece
@@ -44,4 +49,6 @@ struct zr_plan {
 namespace zr {
 // Builds the ZeRO-3 shard bookkeeping and its device tile table (zr_zero3.cu).
 zr_status build_shard_tables(zr_plan* p);
+// Picks the in-place step's kernels and grids once the tile table exists (zr_inplace.cu).
+zr_status init_inplace(zr_plan* p);
 }  // namespace zr

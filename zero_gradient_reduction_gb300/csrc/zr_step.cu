@@ -105,7 +105,8 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
 
   // Kernel for (dtype, W, A) and the number of blocks that fit on the GPU at once.
   const bool f32 = p->fp32_grads != 0;
-  KernelFn k = p->dtype == ZR_F16 ? pick_kernel<zr::DT_F16>(p->W, p->A, f32) : pick_kernel<zr::DT_BF16>(p->W, p->A, f32);
+  KernelFn k = p->dtype == ZR_F16 ? pick_kernel<zr::DT_F16, kPingPong>(p->W, p->A, f32)
+                                  : pick_kernel<zr::DT_BF16, kPingPong>(p->W, p->A, f32);
   p->kernel = reinterpret_cast<void*>(k);
   int per_sm = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&p->device);
@@ -155,6 +156,7 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
     return s;
   }
   zr_status ss = zr::build_shard_tables(p);
+  if (ss == ZR_OK) ss = zr::init_inplace(p);
   if (ss != ZR_OK) {
     zr_plan_destroy(p);
     return ss;
@@ -284,29 +286,7 @@ static zr_status launch_step(zr_plan* p, int stage, const void* const* grads, co
                              const zr_adamw_hyper* h, cudaStream_t s, int64_t tile0, int64_t tile1, int grid,
                              unsigned total) {
   if (tile1 <= tile0 || grid < 1) return ZR_OK;
-  FusedArgs a;
-  std::memset(&a, 0, sizeof a);
-  for (int r = 0; r < p->W * p->A; ++r) a.grads[r] = grads[r];
-  for (int i = 0; i < p->W; ++i) a.order[i] = p->order[i];
-  a.tiles = p->tiles_dev;
-  a.tile0 = tile0;
-  a.tile1 = tile1;
-  a.total_blocks = total;
-  for (int k = 0; k < 2; ++k) {
-    a.master[k] = st->master[k];
-    a.m[k] = st->m[k];
-    a.v[k] = st->v[k];
-    a.param[k] = static_cast<uint16_t*>(st->param[k]);
-  }
-  a.ctrl = p->ctrl_dev;
-  a.lr = h->lr;
-  a.beta1 = h->beta1;
-  a.beta2 = h->beta2;
-  a.eps = h->eps;
-  a.weight_decay = h->weight_decay;
-  a.W = p->W;
-  a.A = p->A;
-  a.stage = stage;
+  const FusedArgs a = make_args(p, stage, grads, st->master, st->m, st->v, st->param, h, tile0, tile1, total);
   reinterpret_cast<KernelFn>(p->kernel)<<<grid, kThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ZR_OK : fail(ZR_ERR_CUDA, "zr_step: launch failed: %s", cudaGetErrorString(e));
