@@ -65,9 +65,10 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def _traffic_record(workload: str):
-    """Per-launch DRAM bytes of the fused kernel from the committed ncu summary, if the kernel source has
-    not changed since it was taken (the summary records the source hash)."""
+def _traffic_record(workload: str, prefix: str = "fused_step", key: str = "traffic_bytes_per_launch"):
+    """DRAM bytes of the fused kernel per launch (or of the in-place step's two launches, per step) from the
+    committed ncu summary, if the kernel source has not changed since it was taken (the summary records the
+    source hash)."""
     import hashlib
     src = os.path.join(ROOT, "zero_gradient_reduction_gb300", "csrc")
     h = hashlib.sha256()
@@ -75,7 +76,7 @@ def _traffic_record(workload: str):
         with open(os.path.join(src, f), "rb") as fh:
             h.update(fh.read())
     digest = h.hexdigest()[:16]
-    path = os.path.join(ROOT, "profiles", f"fused_step_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{prefix}_{workload}.md")
     if not os.path.exists(path):
         return None, digest
     rec = {}
@@ -87,7 +88,7 @@ def _traffic_record(workload: str):
     if rec.get("kernel_source_sha256_16") != digest:
         return None, digest
     try:
-        return float(rec["traffic_bytes_per_launch"]), digest
+        return float(rec[key]), digest
     except Exception:
         return None, digest
 
@@ -228,11 +229,13 @@ def run_reference(args, w):
     return 0
 
 
-def _config(w, buckets, l2_note, launch=None):
+def _config(w, buckets, l2_note, launch=None, inplace=False):
     cfg = {"workload": f"{w.name}: {w.description}", "W": w.W, "A": w.A, "stage": w.stage,
            "params": w.n, "buckets": int(len(buckets)), "grad_dtype": "fp16" if w.dtype == 0 else "bf16",
-           "state_dtype": "fp32 master/m/v (ping-pong sets)",
-           "alg_bytes_per_param": w.alg_bytes_per_param(), "l2": l2_note, "parallelism": "replicas"}
+           "state_dtype": "fp32 master/m/v (one set, updated in place)" if inplace else
+           "fp32 master/m/v (ping-pong sets)",
+           "alg_bytes_per_param": w.alg_bytes_per_param() + (2 * w.W * w.A if inplace else 0), "l2": l2_note,
+           "parallelism": "replicas"}
     if launch:
         cfg["launch"] = launch
     return cfg
@@ -323,10 +326,18 @@ def run_zr(args, w):
     cs = stream.cuda_stream
     table = torch.from_numpy(zrgen.normal_table().copy()).to(dev)
     n = plan.numel
-    state = plan.new_state(dev)
-    state.master[0].zero_()
-    layout.master_dev(state.master[0], table, cs)
-    zr.all_gather(state.master[0], [state.param[0]])
+    # the main step: ping-pong sets (zr_step), or one set stepped in place (zr_step_inplace) for a workload
+    # whose two sets do not fit, or on request
+    inplace_main = args.inplace or w.state_sets == 1
+    if inplace_main:
+        state = plan.new_state1(dev)
+        master0, param0 = state.master, state.param
+    else:
+        state = plan.new_state(dev)
+        master0, param0 = state.master[0], state.param[0]
+    master0.zero_()
+    layout.master_dev(master0, table, cs)
+    zr.all_gather(master0, [param0])
     grads = [torch.zeros(n, dtype=plan.torch_dtype(), device=dev) for _ in range(w.W * w.A)]
     for r in range(w.W * w.A):
         layout.grads_dev(grads[r], 1, r, w.init_scale, table, cs)
@@ -340,7 +351,7 @@ def run_zr(args, w):
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(k):
-            graph.replay()  # one fused-step launch
+            graph.replay()  # one fused-step launch (two in place)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         if ws > 1:
@@ -348,7 +359,10 @@ def run_zr(args, w):
         return e0.elapsed_time(e1)
 
     for _ in range(args.warmup):
-        plan.step(grads, state, hyper, stream=stream)
+        if inplace_main:
+            plan.step_inplace(grads, state, hyper, stream=stream)
+        else:
+            plan.step(grads, state, hyper, stream=stream)
     torch.cuda.synchronize(dev)
     # the step as a one-launch CUDA graph, so small workloads are not bound by host launch overhead
     graph = plan.capture(grads, state, hyper)
@@ -371,16 +385,21 @@ def run_zr(args, w):
     ms_step = ms_max / args.steps
     value = whole_job_rate(plan.n_real, ms_step * 1e-3, ws)
 
-    # roofline of the fused kernel: one launch per step, algorithmic bytes (2*W*A + 26) per param
+    # roofline of the fused kernel: one launch per step, algorithmic bytes (2*W*A + 26) per param; in place,
+    # of the step's two launches together, (4*W*A + 26) per param
     peak, peak_kind = _peaks()
-    achieved = rep.bytes_alg / (ms_total / args.steps * 1e-3) / 1e9
-    traffic, _digest = _traffic_record(w.name)
+    step_bytes = rep.bytes_alg + (2 * w.W * w.A * plan.n_real if inplace_main else 0)
+    achieved = step_bytes / (ms_total / args.steps * 1e-3) / 1e9
+    if inplace_main:
+        traffic, _digest = _traffic_record(w.name, "inplace_step", "traffic_bytes_per_step")
+    else:
+        traffic, _digest = _traffic_record(w.name)
 
     # the in-place step (zr_step_inplace: a flag pass, then AdamW in place on ONE state set, for runs with
     # no room for a second set), timed right after the step it is compared with, on the live set of the
     # ping-pong state so that it needs no memory of its own: (4*W*A + 26) bytes per param, two launches
     inplace = None
-    if not args.no_chain:
+    if not args.no_chain and not inplace_main:
         k = plan.report(stream).current
         one = zr.State1.of(state.master[k], state.m[k], state.v[k], state.param[k])
         for _ in range(3):
@@ -409,7 +428,8 @@ def run_zr(args, w):
     # comparison point: the same step as the unfused chain of standalone calls (reduce-scatter per bucket
     # into fp32 sums, flag pass + AdamW in place, cast/all-gather), (2W + 38) bytes per param
     chain = None
-    if w.A == 1 and not args.no_chain:
+    side = not args.no_chain and not inplace_main  # the side measurements use the ping-pong sets
+    if w.A == 1 and side:
         sums = torch.empty(n, dtype=torch.float32, device=dev)
         flag = torch.zeros(1, dtype=torch.int32, device=dev)
         k = rep.current
@@ -439,7 +459,7 @@ def run_zr(args, w):
                  "launches_per_step": len(plan.buckets) + 3,
                  "calls": "zr_reduce_scatter per bucket, zr_adamw_shard_step, zr_all_gather"}
         del sums
-    if w.A > 1 and not args.no_chain:
+    if w.A > 1 and side:
         # the standalone accumulate path: A zr_accumulate passes per worker into fp32, then the step on the
         # fp32 sums (W*(2A + 4(A-1) + 4A) + 4W + 26 bytes per param against 2WA + 26 fused)
         acc_plan = zr.Plan(list(w.tensors), W=w.W, A=1, dtype=w.dtype, stage=w.stage, cap=w.cap,
@@ -474,7 +494,7 @@ def run_zr(args, w):
     # ZeRO-3: the parameter all-gather before each layer's forward/backward, bucket by bucket, from the W
     # shards into a transient replica (2 bytes read + 2 written per param)
     zero3 = None
-    if not args.no_chain:
+    if side:
         shards = plan.new_shards(dev)
         plan.shard_params(state.param[rep.current], shards, stream=stream)
         transient = torch.empty_like(state.param[0])
@@ -500,11 +520,11 @@ def run_zr(args, w):
         del shards, transient
 
     overlap = None
-    if not args.no_chain and w.A == 1:
+    if side and w.A == 1:
         overlap = measure_overlap(torch, zr, plan, grads, state, hyper, dev, stream)
 
     offload = None
-    if not args.no_chain and w.A == 1 and ws == 1:
+    if side and w.A == 1 and ws == 1:
         # ZeRO-Offload: reduce-scatter on the GPU, AdamW on the host cores over host-resident fp32 state,
         # 4 B/param of sums down and 2 B/param of parameters back over the host link
         nthreads = os.cpu_count() or 8
@@ -535,19 +555,31 @@ def run_zr(args, w):
         host = [torch.empty(n, dtype=plan.torch_dtype(), pin_memory=True) for _ in range(w.W * w.A)]
         for r in range(w.W * w.A):
             host[r].copy_(grads[r])
-        dgr = [torch.empty_like(g) for g in grads]
-        plan.step_from_host(host, dgr, state, hyper, stream=stream)  # warm
+        if inplace_main:
+            # one set in place: the pinned host gradients are copied into the device replicas (one
+            # cudaMemcpyAsync each, on the step's stream), then zr_step_inplace reads them twice in HBM
+            def e2e_step():
+                for r in range(w.W * w.A):
+                    grads[r].copy_(host[r], non_blocking=True)
+                return plan.step_inplace(grads, state, hyper, stream=stream, report=True)
+            api = "pinned host grads copied to the device replicas, zr_step_inplace, report read back"
+        else:
+            dgr = [torch.empty_like(g) for g in grads]
+
+            def e2e_step():
+                return plan.step_from_host(host, dgr, state, hyper, stream=stream)
+            api = "zr_step_from_host (pinned host grads -> device, fused step, report read back)"
+        e2e_step()  # warm
         if ws > 1:
             torch.distributed.barrier()
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
-            r = plan.step_from_host(host, dgr, state, hyper, stream=stream)
+            r = e2e_step()
         dt = max_over_ranks(time.perf_counter() - t0, ws, dev)
         e2e = {"value": whole_job_rate(plan.n_real * args.e2e_steps, dt, ws), "unit": "Gparams/s",
                "h2d_bytes_per_step": int(2 * n * w.W * w.A), "d2h_bytes_per_step": int(__import__("ctypes").sizeof(r)),
-               "ms_per_step": dt / args.e2e_steps * 1e3, "steps": args.e2e_steps,
-               "api": "zr_step_from_host (pinned host grads -> device, fused step, report read back)"}
-        del host, dgr
+               "ms_per_step": dt / args.e2e_steps * 1e3, "steps": args.e2e_steps, "api": api}
+        del host
 
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         params, secs, what = oracle_sample(w, plan.buckets, plan.tensor_offsets, args.cpu_seconds)
@@ -559,15 +591,18 @@ def run_zr(args, w):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded Philox4x32-10 normal draws, the workload's shapes and sigmas)",
-        "config": _config(w, plan.buckets, f"inputs larger than L2: {rep.bytes_alg / 1e9:.1f} GB moved per step"
-                          if rep.bytes_alg > 4 * 129e6 else
-                          f"{rep.bytes_alg / 1e6:.0f} MB per step: L2-resident, reported, not an HBM figure",
-                          launch="zr_step captured once as a CUDA graph, replayed once per timed step"),
+        "config": _config(w, plan.buckets, f"inputs larger than L2: {step_bytes / 1e9:.1f} GB moved per step"
+                          if step_bytes > 4 * 129e6 else
+                          f"{step_bytes / 1e6:.0f} MB per step: L2-resident, reported, not an HBM figure",
+                          launch="zr_step_inplace (flag pass + update) captured once as a CUDA graph, replayed once "
+                          "per timed step" if inplace_main else
+                          "zr_step captured once as a CUDA graph, replayed once per timed step", inplace=inplace_main),
         "hbm_tbs": achieved / 1e3,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_kind} HBM copy bandwidth",
                      "frac_of_8tbs_nominal": achieved / 8000.0,
-                     "kernel": "fused_step_kernel (one launch per step)"},
+                     "kernel": "fused_step_kernel flag pass + in-place update (bytes and time of the step's two "
+                               "launches together)" if inplace_main else "fused_step_kernel (one launch per step)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "unfused_chain": chain,
@@ -575,7 +610,7 @@ def run_zr(args, w):
         "inplace_step": inplace,
         "bucketed_overlap": overlap,
         "zero_offload": offload,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if inplace_main else 1),
         "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
                    "reasons": clocks.get("reasons"), "samples": clocks.get("samples"),
                    "power_w_max": clocks.get("power_w_max"), "attempts": attempts},
@@ -601,6 +636,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chain", action="store_true")
     ap.add_argument("--chain-steps", type=int, default=5)
+    ap.add_argument("--inplace", action="store_true",
+                    help="time zr_step_inplace on one state set as the main step (always so for 13b)")
     args = ap.parse_args()
     if args.warmup < 3:
         print(f"bench: raising --warmup {args.warmup} to the minimum of 3", file=sys.stderr)

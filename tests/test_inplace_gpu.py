@@ -143,3 +143,98 @@ def test_inplace_error_paths():
     s1.master.zero_()
     r = plan.step_inplace(grads, s1, HYPER, report=True)
     assert r.t == 1 and r.steps == 1 and r.overflow == 0
+
+
+def test_inplace_guard_bands_clean_and_skipped():
+    """Both launches stay inside every buffer, on a clean step and on a skipped one."""
+    from test_guards_gpu import Guarded
+    numels = [12_345, 7, 40_000, 8, 999]
+    for W, A in ((3, 1), (2, 4), (8, 1)):
+        plan = zr.Plan(numels, W=W, A=A, dtype=zr.BF16, stage=2, cap=20_000, scaler=zr.Scaler(1.0))
+        n = plan.numel
+        grads = [Guarded(n, torch.bfloat16) for _ in range(W * A)]
+        for g in grads:
+            g.t.normal_()
+        bufs = [Guarded(n, torch.float32) for _ in range(3)] + [Guarded(n, torch.bfloat16)]
+        bufs[0].t.fill_(0.01)
+        bufs[1].t.zero_()
+        bufs[2].t.zero_()
+        one = zr.State1.of(*(b.t for b in bufs))
+        rep = plan.step_inplace([g.t for g in grads], one, HYPER, report=True)
+        assert rep.overflow == 0
+        grads[-1].t[n - 1] = float("nan")
+        rep = plan.step_inplace([g.t for g in grads], one, HYPER, report=True)
+        assert rep.overflow == 1 and rep.t == 1
+        assert all(x.intact() for x in grads + bufs), (W, A)
+        plan.close()
+
+
+def test_inplace_max_workers_and_replicas_with_empty_tensors():
+    """W = 64 and W*A = 256 (the limits), zero-size tensors in the list."""
+    import oracle
+    from test_parity_gpu import OHYPER, assert_state_close
+    numels = [0, 5000, 0, 1, 20_000, 0]
+    for W, A in ((64, 1), (64, 4)):
+        plan = zr.Plan(numels, W=W, A=A, dtype=zr.BF16, stage=1, cap=8_000, scaler=zr.Scaler(1.0))
+        n = plan.numel
+        rng = np.random.default_rng(W * 3 + A)
+        hg = [oracle.encode(zr.BF16, rng.normal(size=n).astype(np.float32)) for _ in range(W * A)]
+        grads = [torch.from_numpy(g.view(np.int16).copy()).cuda().view(torch.bfloat16) for g in hg]
+        one = plan.new_state1()
+        master = (rng.normal(size=n) * 0.02).astype(np.float32)
+        one.master.copy_(torch.from_numpy(master))
+        rep = plan.step_inplace(grads, one, HYPER, report=True)
+        o = [master.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16)]
+        orep, _ = oracle.step(W, A, zr.BF16, plan.buckets, hg, *o, OHYPER, oracle.new_scaler(1.0))
+        assert rep.overflow == orep.overflow == 0 and rep.t == 1
+        assert_state_close(one.master.cpu().numpy(), one.m.cpu().numpy(), one.v.cpu().numpy(),
+                           one.param.cpu().view(torch.int16).numpy().view(np.uint16), *o, exact=True,
+                           where=f"in place W={W} A={A}: ")
+        plan.close()
+
+
+def test_inplace_fp32_overflow_from_finite_bf16_skips():
+    """Finite bf16 values whose fp32 ring sum is +inf: the flag pass must see the sum, not the inputs."""
+    import oracle
+    n = 64
+    hg = [oracle.encode(zr.BF16, np.full(n, 3.0e38, np.float32)) for _ in range(2)]
+    plan = zr.Plan([n], W=2, dtype=zr.BF16, stage=2, cap=n, scaler=zr.Scaler(1.0, dynamic=True))
+    one = plan.new_state1()
+    one.master.fill_(0.5)
+    one.param.fill_(0.5)
+    before = [t.clone() for t in (one.master, one.m, one.v, one.param)]
+    grads = [torch.from_numpy(g.view(np.int16).copy()).cuda().view(torch.bfloat16) for g in hg]
+    rep = plan.step_inplace(grads, one, HYPER, report=True)
+    assert rep.overflow == 1 and rep.t == 0 and rep.skipped_total == 1
+    for a, b in zip((one.master, one.m, one.v, one.param), before):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    plan.close()
+
+
+@pytest.mark.parametrize("W,A", [(2, 4), (8, 2)])
+def test_inplace_fp32_gradients_equal_pingpong(W, A):
+    """A plan over fp32 micro-batch sums (zr_accumulate): in place and ping-pong give the same bytes."""
+    numels = [40_000, 999, 77_777, 8]
+    rng = np.random.default_rng(W + 5 * A)
+    order = list(rng.permutation(W))
+    kw = dict(W=W, A=1, dtype=zr.BF16, stage=2, cap=50_000, order=order, scaler=zr.Scaler(1.0), fp32_grads=True)
+    pa, pb = zr.Plan(numels, **kw), zr.Plan(numels, **kw)
+    n = pa.numel
+    st = pa.new_state()
+    st.master[0].copy_(torch.from_numpy((rng.normal(size=n) * 0.02).astype(np.float32)))
+    one = pb.new_state1()
+    one.master.copy_(st.master[0])
+    accs = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(W)]
+    for step in (1, 2, 3):
+        for wk in range(W):
+            for q in range(A):
+                g = torch.from_numpy((rng.normal(size=n) * 1e-2).astype(np.float32)).cuda().to(torch.bfloat16)
+                zr.accumulate(g, accs[wk], q == 0)
+        ra = pa.step(accs, st, HYPER, report=True)
+        rb = pb.step_inplace(accs, one, HYPER, report=True)
+        assert ra.overflow == rb.overflow == 0 and ra.t == rb.t == step
+        L = st.live(ra.current)
+        for x, y in zip((L["master"], L["m"], L["v"], L["param"]), (one.master, one.m, one.v, one.param)):
+            assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), step
+    pa.close()
+    pb.close()

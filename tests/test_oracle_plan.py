@@ -49,6 +49,16 @@ def test_flat_7b_in_200m_buckets():
     assert all(int(c) == 100_000_000 for c in b[:, 2])
 
 
+def test_flat_13b_in_200m_buckets_and_its_memory():
+    """The 13B in-place workload: 65 full buckets; its two ping-pong sets would not fit one GB300 (288 GB)
+    beside the gradients, one set does."""
+    w = zrgen.workload("13b")
+    b, _ = oracle.bucket_plan(list(w.tensors), w.cap, w.W)
+    assert len(b) == 65 and int(b[:, 1].sum()) == 13_000_000_000 and w.state_sets == 1
+    grads = 2 * w.W * w.A * w.n
+    assert grads + 2 * 14 * w.n > 288e9 > grads + 14 * w.n
+
+
 def test_contiguous_reverse_and_aligned():
     rng = np.random.default_rng(0)
     for trial in range(20):

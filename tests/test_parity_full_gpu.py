@@ -95,9 +95,17 @@ def run_sampled(w: zrgen.Workload, steps=None, extra_buckets=3, inplace=False):
         S = rep.scale
     final = plan.report()
     plan.close()
-    del grads, state
+    del grads, state, live, master0
     torch.cuda.empty_cache()
     return final
+
+
+def free_bytes() -> int:
+    """Device bytes free once every buffer of the earlier tests is released (not held in torch's cache)."""
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+    return torch.cuda.mem_get_info()[0]
 
 
 def test_gpt2_full_size():
@@ -112,7 +120,7 @@ def test_1p3b_full_size():
 
 def test_7b_full_size_with_overflow_skip():
     w = zrgen.workload("7b")
-    free, _ = torch.cuda.mem_get_info()
+    free = free_bytes()
     need = w.n * (2 * w.W + 2 * 14) + (8 << 30)
     if free < need:
         pytest.skip(f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}")
@@ -129,12 +137,24 @@ def test_1p3b_full_size_in_place():
 def test_7b_full_size_in_place_with_overflow_skip():
     """One state set: 14 bytes per parameter less than the ping-pong sets (126 GB in all instead of 224)."""
     w = zrgen.workload("7b")
-    free, _ = torch.cuda.mem_get_info()
+    free = free_bytes()
     need = w.n * (2 * w.W + 14) + (8 << 30)
     if free < need:
         pytest.skip(f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}")
     rep = run_sampled(w, inplace=True)
     assert rep.t == 5 and rep.scale == 32768.0 and rep.skipped_total == 1 and rep.steps == 6
+
+
+def test_13b_full_size_in_place_with_overflow_skip():
+    """A model whose ping-pong sets would not fit (416 GB): one set, stepped in place (234 GB in all)."""
+    w = zrgen.workload("13b")
+    free = free_bytes()
+    need = w.n * (2 * w.W + 14) + (8 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 1e9:.0f} GB free, have {free / 1e9:.0f}")
+    rep = run_sampled(w, inplace=True)
+    assert rep.t == 5 and rep.scale == 32768.0 and rep.skipped_total == 1 and rep.steps == 6
+    assert rep.n_real == 13_000_000_000
 
 
 @pytest.mark.parametrize("name", ["sweep_W2_cap2^19", "sweep_W4_cap2^23", "sweep_W8_cap2^28"])

@@ -64,6 +64,7 @@ class Workload:
     master_sigma: float = 0.02
     align: int = 8
     description: str = ""
+    state_sets: int = 2                # 2 = ping-pong sets (zr_step); 1 = one set updated in place only
 
     @property
     def n(self) -> int:
@@ -96,6 +97,13 @@ WORKLOADS = {
                    sigma=1e-2, init_scale=65536.0, dynamic=True, inject_step=3,
                    description="flat 7.0e9 params in 200M-param buckets, W=2, fp16, dynamic loss scale S0=65536, "
                                "+inf injected at step 3"),
+    # a model whose ping-pong state sets do not fit one GPU (1.3e10 x 32 B = 416 GB) but whose in-place step does
+    # (1.3e10 x 18 B = 234 GB): the 13B size that ZeRO-Offload is said to train on a single GPU (page
+    # "并行训练框架DeepSpeed介绍", (16) ZeRO-Offload), here with all of the optimizer state in HBM
+    "13b": Workload("13b", _flat(13_000_000_000, 65), W=2, A=1, dtype=0, stage=1, cap=200_000_000, steps=6, seed=0,
+                    sigma=1e-2, init_scale=65536.0, dynamic=True, inject_step=3, state_sets=1,
+                    description="flat 1.3e10 params in 200M-param buckets, W=2, fp16, dynamic loss scale S0=65536, "
+                                "+inf injected at step 3, one state set stepped in place"),
     # the 7B workload's kernel configuration (W=2, fp16, 200M-param buckets) at 1/35 of its size: a case small
     # enough for a full profiler capture
     "7b_slice": Workload("7b_slice", _flat(200_000_000, 1), W=2, A=1, dtype=0, stage=1, cap=200_000_000, steps=6,
