@@ -17,20 +17,6 @@ using zr::fail;
 #include "zr_plan.h"
 #include "zr_step_kernel.cuh"
 
-namespace {
-
-// Blocks of `k` that fit on the GPU at once, capped at the plan's tile count.
-cudaError_t grid_for(const zr_plan* p, KernelFn k, int* grid) {
-  int per_sm = 0, sms = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, 0);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
-  const int64_t full = (int64_t)(sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
-  *grid = (int)(p->ntiles < full ? (p->ntiles > 0 ? p->ntiles : 1) : full);
-  return e;
-}
-
-}  // namespace
-
 zr_status zr::init_inplace(zr_plan* p) {
   const bool f32 = p->fp32_grads != 0;
   const bool f16 = p->dtype == ZR_F16;
@@ -40,9 +26,9 @@ zr_status zr::init_inplace(zr_plan* p) {
                    : pick_kernel<zr::DT_BF16, kInPlace>(p->W, p->A, f32);
   p->ip_flag_kernel = reinterpret_cast<void*>(f);
   p->ip_update_kernel = reinterpret_cast<void*>(u);
-  cudaError_t e = grid_for(p, f, &p->ip_flag_grid);
-  if (e == cudaSuccess) e = grid_for(p, u, &p->ip_update_grid);
-  return e == cudaSuccess ? ZR_OK : fail(ZR_ERR_CUDA, "zr_plan_create: %s", cudaGetErrorString(e));
+  p->ip_flag_grid = zr::step_grid(p, p->ntiles);
+  p->ip_update_grid = zr::step_grid(p, p->ntiles);
+  return ZR_OK;
 }
 
 extern "C" zr_status zr_step_inplace(zr_plan* p, int stage, const void* const* grads, const zr_state1* st,

@@ -22,6 +22,7 @@ struct zr_plan {
   zr::Ctrl* ctrl_dev = nullptr;
   void* kernel = nullptr;  // the fused_step_kernel instantiation for (dtype, W, A)
   int grid = 0;
+  int64_t resident = 0;    // blocks of that kernel that fit on the GPU at once
   int device = 0;
   // bucketed launches (zr_step_bucket): bucket b's tiles are [tile_begin[b], tile_begin[b+1]),
   // launched with bucket_grid[b] blocks; a step's launches add up to bucket_blocks blocks
@@ -29,7 +30,7 @@ struct zr_plan {
   std::vector<int> bucket_grid;
   unsigned bucket_blocks = 0;
   // in-place step (zr_step_inplace): the flag-pass and in-place instantiations for
-  // (dtype, W, A), each with the number of blocks that fit on the GPU at once
+  // (dtype, W, A) and their grids (one block per tile)
   void* ip_flag_kernel = nullptr;
   void* ip_update_kernel = nullptr;
   int ip_flag_grid = 0, ip_update_grid = 0;
@@ -51,4 +52,17 @@ namespace zr {
 zr_status build_shard_tables(zr_plan* p);
 // Picks the in-place step's kernels and grids once the tile table exists (zr_inplace.cu).
 zr_status init_inplace(zr_plan* p);
+
+// Blocks for a launch over `ntiles` tiles. A large launch gets one block per tile: the
+// hardware hands blocks out in index order as earlier ones finish, so the tiles in flight
+// stay a compact window of the address space and every block ends within one tile of the
+// others (a persistent grid striding over the tiles measured 3-9 % slower on the 1.3B and
+// 7B workloads). Under four waves of tiles a persistent grid of at most `resident` blocks
+// striding over them avoids a last, partly filled wave.
+inline int step_grid(const zr_plan* p, int64_t ntiles) {
+  constexpr int64_t kMaxBlocks = 1 << 30;  // a step's launches stay below 2^32 blocks
+  if (ntiles < 1) return 1;
+  if (ntiles >= 4 * p->resident) return (int)(ntiles < kMaxBlocks ? ntiles : kMaxBlocks);
+  return (int)(ntiles < p->resident ? ntiles : p->resident);
+}
 }  // namespace zr

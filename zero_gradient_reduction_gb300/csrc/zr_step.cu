@@ -103,7 +103,7 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   for (int t = 0; t < d->ntensors; ++t) p->n_real += d->numels[t];
   p->numel = nb ? p->buckets.back().start + p->buckets.back().len : 0;
 
-  // Kernel for (dtype, W, A) and the number of blocks that fit on the GPU at once.
+  // Kernel for (dtype, W, A) and the number of its blocks that fit on the GPU at once.
   const bool f32 = p->fp32_grads != 0;
   KernelFn k = p->dtype == ZR_F16 ? pick_kernel<zr::DT_F16, kPingPong>(p->W, p->A, f32)
                                   : pick_kernel<zr::DT_BF16, kPingPong>(p->W, p->A, f32);
@@ -115,9 +115,10 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   if (per_sm < 1) per_sm = 1;
   const int64_t full = (int64_t)(sms > 0 ? sms : 1) * per_sm;
 
-  // Tile schedule: every block of every bucket cut into pieces of at most `tile` elements.
-  // Large plans use kTileElems; a small plan halves the tile (down to 2048 elements)
-  // until it has at least two tiles for every resident block, so that it fills the GPU.
+  // Tile schedule: every block of every bucket cut into pieces of at most `tile` elements,
+  // one thread block per tile. Large plans use kTileElems; a small plan halves the tile
+  // (down to 2048 elements) until it has at least two tiles for every block that fits on
+  // the GPU at once, so that it fills the GPU.
   int64_t tile = kTileElems;
   while (tile > 2048 && p->numel / tile < 2 * full) tile /= 2;
   std::vector<int4> tiles;
@@ -136,10 +137,10 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   }
   p->ntiles = (int64_t)tiles.size();
   p->tile_begin.push_back(p->ntiles);
-  p->grid = (int)(p->ntiles < full ? (p->ntiles > 0 ? p->ntiles : 1) : full);
+  p->resident = full;
+  p->grid = zr::step_grid(p, p->ntiles);
   for (size_t b = 0; b + 1 < p->tile_begin.size(); ++b) {
-    const int64_t nt = p->tile_begin[b + 1] - p->tile_begin[b];
-    p->bucket_grid.push_back((int)(nt < full ? nt : full));
+    p->bucket_grid.push_back(zr::step_grid(p, p->tile_begin[b + 1] - p->tile_begin[b]));
     p->bucket_blocks += (unsigned)p->bucket_grid.back();
   }
   if (e == cudaSuccess && !tiles.empty()) e = cudaMalloc(&p->tiles_dev, tiles.size() * sizeof(int4));

@@ -18,7 +18,7 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTileElems = 16384;  // elements per tile (a multiple of 8 * kThreads)
+constexpr int kTileElems = 32768;  // elements per tile (a multiple of 8 * kThreads)
 
 enum : int { kPingPong = 0, kFlagPass = 1, kInPlace = 2 };
 
