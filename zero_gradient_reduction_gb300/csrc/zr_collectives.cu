@@ -16,20 +16,27 @@ namespace {
 
 constexpr int kThreads = 256;
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-  }
-  return n;
+// Work is cut into chunks of kChunkElems consecutive elements, one block per chunk (a
+// block moves on to chunk + gridDim.x only if the grid was capped). The hardware hands
+// blocks out in index order, so the elements in flight stay a compact window of every
+// array; a grid-stride loop would spread each block's accesses over the whole array.
+constexpr int64_t kChunkElems = 32768;
+
+// Blocks for n elements.
+int chunk_grid(int64_t n) {
+  int64_t want = (n + kChunkElems - 1) / kChunkElems;
+  if (want < 1) want = 1;
+  return (int)(want < (1 << 30) ? want : (1 << 30));
 }
 
-int grid_for(int64_t work_items, int per_sm = 8) {
-  int64_t want = (work_items + kThreads - 1) / kThreads;
-  int64_t cap = (int64_t)sm_count() * per_sm;
-  if (want < 1) want = 1;
-  return (int)(want < cap ? want : cap);
+// Calls f(i) for this block's items of PER elements each, out of nitems.
+template <int PER, class F>
+__device__ __forceinline__ void for_block_items(int64_t nitems, F&& f) {
+  constexpr int64_t kItems = kChunkElems / PER;
+  for (int64_t c = blockIdx.x; c * kItems < nitems; c += gridDim.x) {
+    const int64_t end = (c + 1) * kItems < nitems ? (c + 1) * kItems : nitems;
+    for (int64_t i = c * kItems + threadIdx.x; i < end; i += blockDim.x) f(i);
+  }
 }
 
 zr_status launch_status(const char* what) {
@@ -65,8 +72,7 @@ __global__ void __launch_bounds__(kThreads) rs_kernel(const __grid_constant__ Rs
   const int W = WT > 0 ? WT : a.W;
   bool bad = false;
   const int64_t ngroups = (a.n + 7) / 8;
-  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < ngroups;
-       g += (int64_t)gridDim.x * blockDim.x) {
+  for_block_items<8>(ngroups, [&](int64_t g) {
     const int64_t e = g * 8;
     const int c = (int)(e / a.C);
     if (e + 8 <= a.n) {
@@ -112,7 +118,7 @@ __global__ void __launch_bounds__(kThreads) rs_kernel(const __grid_constant__ Rs
         a.sums[i] = s;
       }
     }
-  }
+  });
   block_flag_or(bad, a.overflow);
 }
 
@@ -133,10 +139,10 @@ __global__ void __launch_bounds__(kThreads) flag_pass_kernel(const float* __rest
                                                               int32_t* overflow) {
   bool bad = false;
   const int64_t nv = n / 4;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nv; i += (int64_t)gridDim.x * blockDim.x) {
+  for_block_items<4>(nv, [&](int64_t i) {
     float4 v = zr::ld_once_f4(x + 4 * i);
     bad |= zr::nonfinite(v.x) | zr::nonfinite(v.y) | zr::nonfinite(v.z) | zr::nonfinite(v.w);
-  }
+  });
   for (int64_t i = nv * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
     bad |= zr::nonfinite(x[i]);
   block_flag_or(bad, overflow);
@@ -159,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) adamw_kernel(const __grid_constant__
   __syncthreads();
   if (s_skip) return;
   const int64_t nv = a.n / 4;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nv; i += (int64_t)gridDim.x * blockDim.x) {
+  for_block_items<4>(nv, [&](int64_t i) {
     const int64_t e = 4 * i;
     float4 s = zr::ld_once_f4(a.sums + e), p = zr::ld_once_f4(a.master + e), m = zr::ld_once_f4(a.m + e),
            v = zr::ld_once_f4(a.v + e);
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) adamw_kernel(const __grid_constant__
     zr::st_once_f4(a.master + e, p);
     zr::st_once_f4(a.m + e, m);
     zr::st_once_f4(a.v + e, v);
-  }
+  });
   for (int64_t i = nv * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < a.n;
        i += (int64_t)gridDim.x * blockDim.x) {
     float p = a.master[i], m = a.m[i], v = a.v[i];
@@ -192,8 +198,7 @@ struct AgArgs {
 template <int DT>
 __global__ void __launch_bounds__(kThreads) ag_kernel(const __grid_constant__ AgArgs a) {
   const int64_t ngroups = (a.n + 7) / 8;
-  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < ngroups;
-       g += (int64_t)gridDim.x * blockDim.x) {
+  for_block_items<8>(ngroups, [&](int64_t g) {
     const int64_t e = g * 8;
     if (e + 8 <= a.n) {
       float4 lo = zr::ld_once_f4(a.master + e), hi = zr::ld_once_f4(a.master + e + 4);
@@ -206,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) ag_kernel(const __grid_constant__ Ag
         for (int r = 0; r < a.R; ++r) static_cast<uint16_t*>(a.out[r])[i] = b;
       }
     }
-  }
+  });
 }
 
 }  // namespace
@@ -264,7 +269,7 @@ extern "C" zr_status zr_reduce_scatter(const void* const* grads, zr_dtype dt, in
   a.C = zr_chunk_size(n, W, ZR_ALIGN);
   a.W = W;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int grid = grid_for((n + 7) / 8);
+  const int grid = chunk_grid(n);
   if (dt == ZR_F16) launch_rs<zr::DT_F16>(a, grid, s);
   else if (dt == ZR_BF16) launch_rs<zr::DT_BF16>(a, grid, s);
   else launch_rs<zr::DT_F32>(a, grid, s);
@@ -277,7 +282,7 @@ template <int DT, bool FIRST>
 __global__ void __launch_bounds__(kThreads) accumulate_kernel(const void* __restrict__ g, float* __restrict__ acc,
                                                               int64_t n) {
   const int64_t ngroups = n / 8;
-  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < ngroups; q += (int64_t)gridDim.x * blockDim.x) {
+  for_block_items<8>(ngroups, [&](int64_t q) {
     const int64_t e = q * 8;
     float x[8];
     zr::load8<DT>(g, e, x);
@@ -289,7 +294,7 @@ __global__ void __launch_bounds__(kThreads) accumulate_kernel(const void* __rest
     }
     zr::st_once_f4(acc + e, make_float4(x[0], x[1], x[2], x[3]));
     zr::st_once_f4(acc + e + 4, make_float4(x[4], x[5], x[6], x[7]));
-  }
+  });
   for (int64_t i = ngroups * 8 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float x = zr::load1<DT>(g, i);
@@ -306,7 +311,7 @@ extern "C" zr_status zr_accumulate(const void* grad, zr_dtype dt, float* acc, in
     return fail(ZR_ERR_INVALID, "zr_accumulate: null or misaligned pointer");
   if (n == 0) return ZR_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int grid = grid_for(n / 8 + 1);
+  const int grid = chunk_grid(n);
   if (dt == ZR_F16) {
     if (first) accumulate_kernel<zr::DT_F16, true><<<grid, kThreads, 0, s>>>(grad, acc, n);
     else accumulate_kernel<zr::DT_F16, false><<<grid, kThreads, 0, s>>>(grad, acc, n);
@@ -332,7 +337,7 @@ extern "C" zr_status zr_adamw_shard_step(const float* shard_sums, float* m, floa
     return fail(ZR_ERR_INVALID, "zr_adamw_shard_step: misaligned array");
   if (len == 0) return ZR_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  flag_pass_kernel<<<grid_for(len / 4 + 1), kThreads, 0, s>>>(shard_sums, len, overflow);
+  flag_pass_kernel<<<chunk_grid(len), kThreads, 0, s>>>(shard_sums, len, overflow);
   zr_status st = launch_status("zr_adamw_shard_step flag pass");
   if (st != ZR_OK) return st;
   AdamArgs a{};
@@ -344,7 +349,7 @@ extern "C" zr_status zr_adamw_shard_step(const float* shard_sums, float* m, floa
   a.n = len;
   a.r = (float)(1.0 / ((double)loss_scale * (double)W));
   a.k = zr::adam_consts_host(*h, zr::bias_correction_host(h->beta1, t), zr::bias_correction_host(h->beta2, t));
-  adamw_kernel<<<grid_for(len / 4 + 1), kThreads, 0, s>>>(a);
+  adamw_kernel<<<chunk_grid(len), kThreads, 0, s>>>(a);
   return launch_status("zr_adamw_shard_step update");
 }
 
@@ -366,7 +371,7 @@ extern "C" zr_status zr_all_gather(const float* master, int64_t n, zr_dtype out_
   a.n = n;
   a.R = n_replicas;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int grid = grid_for((n + 7) / 8);
+  const int grid = chunk_grid(n);
   if (out_dt == ZR_F16) ag_kernel<zr::DT_F16><<<grid, kThreads, 0, s>>>(a);
   else ag_kernel<zr::DT_BF16><<<grid, kThreads, 0, s>>>(a);
   return launch_status("zr_all_gather");
