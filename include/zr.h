@@ -25,6 +25,10 @@
  *    Host arrays of device pointers (grads, replicas) are read during the call only.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
  *    stream-ordered and asynchronous unless a report is requested.
+ *  - The steps of one plan (zr_step, zr_step_bucket, zr_step_inplace, zr_step_from_host,
+ *    zr_offload_step) share its device control block: order them on one stream, or with
+ *    events. Plans are independent of each other. Host calls on one plan from several
+ *    threads at once are not supported.
  *  - Errors are returned as zr_status; no exception crosses the ABI. A failed call
  *    launches nothing. zr_last_error() returns a thread-local message for the last
  *    failure on the calling thread. An asynchronous CUDA error from an earlier
