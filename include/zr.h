@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
     ZR_OK = 0,
     ZR_ERR_INVALID = 1,     /* bad argument: null/misaligned pointer, size, W, stage, dtype */
-    ZR_ERR_UNSUPPORTED = 2, /* valid request this build does not handle */
+    ZR_ERR_UNSUPPORTED = 2, /* valid request the library does not handle */
     ZR_ERR_CUDA = 3,        /* a CUDA runtime call failed */
     ZR_ERR_OOM = 4,         /* the library could not allocate its own small buffers */
     ZR_ERR_TIMEOUT = 5      /* reserved: no call waits on the device without a bound */
