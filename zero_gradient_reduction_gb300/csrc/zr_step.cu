@@ -10,6 +10,7 @@
 // (2*W*A + 26) bytes per parameter, no tensor cores (no contraction here).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -115,12 +116,34 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   if (per_sm < 1) per_sm = 1;
   const int64_t full = (int64_t)(sms > 0 ? sms : 1) * per_sm;
 
-  // Tile schedule: every block of every bucket cut into pieces of at most `tile` elements,
-  // one thread block per tile. Large plans use kTileElems; a small plan halves the tile
-  // (down to 2048 elements) until it has at least two tiles for every block that fits on
-  // the GPU at once, so that it fills the GPU.
+  // Tile schedule: every block of every bucket cut into pieces of at most `tile` elements.
+  // A large plan takes kTileElems, one thread block per tile (step_grid). A plan of fewer
+  // than four waves of such tiles runs at most `full` blocks at once and its slowest block
+  // sets the time, so its tile is the multiple of one block iteration (8 * kThreads * U
+  // elements, U groups per thread) up to kTileElems with the fewest waves x iterations
+  // per tile, ties going to the larger tile: no last wave and no iteration runs mostly
+  // empty.
   int64_t tile = kTileElems;
-  while (tile > 2048 && p->numel / tile < 2 * full) tile /= 2;
+  if (p->numel < 4 * full * kTileElems) {
+    const int64_t iter = 8 * kThreads * ((!f32 && p->A == 1 && p->W <= 3) ? 2 : 1);
+    std::vector<int64_t> pieces;
+    for (const zr_bucket& b : p->buckets)
+      for (int c = 0; c < p->W; ++c) {
+        const int64_t end = b.start + b.len;
+        const int64_t lo = std::min(b.start + (int64_t)c * b.chunk, end), hi = std::min(lo + b.chunk, end);
+        if (hi > lo) pieces.push_back(hi - lo);
+      }
+    int64_t best = -1;
+    for (int64_t t = iter; t <= kTileElems && pieces.size() <= 65536; t += iter) {
+      int64_t nt = 0;
+      for (int64_t len : pieces) nt += (len + t - 1) / t;
+      const int64_t cost = (nt + full - 1) / full * (t / iter);
+      if (best < 0 || cost <= best) {
+        best = cost;
+        tile = t;
+      }
+    }
+  }
   std::vector<int4> tiles;
   for (const zr_bucket& b : p->buckets) {
     p->tile_begin.push_back((int64_t)tiles.size());

@@ -61,38 +61,52 @@ __device__ void read_consts(const FusedArgs& a, StepConsts& out) {
   out.k.bc2 = (float)__dsub_rn(1.0, __dmul_rn(p2, (double)a.beta2));
 }
 
-// The loss-scale rule and commit, run by one thread of the last block. In place there
-// is one state set, so a clean step does not flip k.
+// The loss-scale rule and commit, run by one thread of the last block. Every other block
+// is done with the control block by then, so it is read in one round trip of 16-byte
+// loads from L2, updated in registers and written back the same way (a chain of single
+// volatile accesses cost several microseconds on small plans). In place there is one
+// state set, so a clean step does not flip k.
 template <int MODE>
 __device__ void finish_step(const FusedArgs& a) {
-  volatile zr::Ctrl* c = a.ctrl;
-  const int of = c->overflow;
-  float scale = c->scale;
-  c->last_overflow = of;
-  c->scale_used = scale;
-  c->stage = a.stage;
-  c->steps = c->steps + 1;
+  constexpr int kWords = sizeof(zr::Ctrl) / 16;
+  union {
+    zr::Ctrl c;
+    uint4 w[kWords];
+  } u;
+  const uint4* src = reinterpret_cast<const uint4*>(a.ctrl);
+#pragma unroll
+  for (int i = 0; i < kWords; ++i) u.w[i] = __ldcg(src + i);
+  zr::Ctrl& c = u.c;
+  const int of = c.overflow;
+  float scale = c.scale;
+  c.last_overflow = of;
+  c.scale_used = scale;
+  c.stage = a.stage;
+  c.steps = c.steps + 1;
   if (of) {
-    c->skipped = c->skipped + 1;
-    if (c->dynamic) {
-      const float s2 = __fmul_rn(scale, c->backoff);
-      scale = s2 > c->min_scale ? s2 : c->min_scale;
-      c->good = 0;
+    c.skipped = c.skipped + 1;
+    if (c.dynamic) {
+      const float s2 = __fmul_rn(scale, c.backoff);
+      scale = s2 > c.min_scale ? s2 : c.min_scale;
+      c.good = 0;
     }
   } else {
-    c->t = c->t + 1;
-    c->prod1 = __dmul_rn(c->prod1, (double)a.beta1);
-    c->prod2 = __dmul_rn(c->prod2, (double)a.beta2);
-    if (MODE == kPingPong) c->k = 1 - c->k;
-    c->good = c->good + 1;
-    if (c->dynamic && c->good >= c->interval) {
-      scale = __fmul_rn(scale, c->growth);
-      c->good = 0;
+    c.t = c.t + 1;
+    c.prod1 = __dmul_rn(c.prod1, (double)a.beta1);
+    c.prod2 = __dmul_rn(c.prod2, (double)a.beta2);
+    if (MODE == kPingPong) c.k = 1 - c.k;
+    c.good = c.good + 1;
+    if (c.dynamic && c.good >= c.interval) {
+      scale = __fmul_rn(scale, c.growth);
+      c.good = 0;
     }
   }
-  c->scale = scale;
-  c->overflow = 0;
-  c->ticket = 0;
+  c.scale = scale;
+  c.overflow = 0;
+  c.ticket = 0;
+  uint4* dst = reinterpret_cast<uint4*>(a.ctrl);
+#pragma unroll
+  for (int i = 0; i < kWords; ++i) __stcg(dst + i, u.w[i]);
   __threadfence();
 }
 
