@@ -24,7 +24,7 @@ CPP = ["zr_host.cpp", "zr_offload_host.cpp"]
 # the host AdamW of ZeRO-Offload: vectorised (no errno on sqrt), still one rounding per op
 CPP_EXTRA = {"zr_offload_host.cpp": ["-O3", "-fno-math-errno", "-pthread"]}
 HEADERS = [os.path.join(INCLUDE, "zr.h"), os.path.join(CSRC, "zr_internal.h"), os.path.join(CSRC, "zr_device.cuh"),
-           os.path.join(CSRC, "zr_step_kernel.cuh"), os.path.join(CSRC, "zr_plan.h")]
+           os.path.join(CSRC, "zr_step_kernel.cuh"), os.path.join(CSRC, "zr_plan.h"), os.path.join(CSRC, "zr_nvtx.h")]
 
 
 def _nvcc_flags(verbose_ptxas: bool = False):

@@ -9,6 +9,7 @@
 
 #include "zr_device.cuh"
 #include "zr_internal.h"
+#include "zr_nvtx.h"
 
 using zr::fail;
 
@@ -242,6 +243,7 @@ AdamConsts adam_consts_host(const zr_adamw_hyper& h, float bc1, float bc2) {
 
 extern "C" zr_status zr_reduce_scatter(const void* const* grads, zr_dtype dt, int64_t n, int W, const int* order,
                                        float* sums, int32_t* overflow, void* stream) {
+  zr::Range range("zr_reduce_scatter");
   zr::clear_error();
   if (n < 0) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: n < 0");
   if (W < 1 || W > ZR_MAX_W) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: W=%d outside [1, %d]", W, ZR_MAX_W);
@@ -304,6 +306,7 @@ __global__ void __launch_bounds__(kThreads) accumulate_kernel(const void* __rest
 }  // namespace
 
 extern "C" zr_status zr_accumulate(const void* grad, zr_dtype dt, float* acc, int64_t n, int first, void* stream) {
+  zr::Range range("zr_accumulate");
   zr::clear_error();
   if (n < 0) return fail(ZR_ERR_INVALID, "zr_accumulate: n < 0");
   if (dt != ZR_F16 && dt != ZR_BF16) return fail(ZR_ERR_INVALID, "zr_accumulate: dtype must be F16 or BF16");
@@ -325,6 +328,7 @@ extern "C" zr_status zr_accumulate(const void* grad, zr_dtype dt, float* acc, in
 extern "C" zr_status zr_adamw_shard_step(const float* shard_sums, float* m, float* v, float* master, int64_t len,
                                          const zr_adamw_hyper* h, float loss_scale, int W, int64_t t,
                                          int32_t* overflow, void* stream) {
+  zr::Range range("zr_adamw_shard_step");
   zr::clear_error();
   if (len < 0) return fail(ZR_ERR_INVALID, "zr_adamw_shard_step: len < 0");
   if (!h) return fail(ZR_ERR_INVALID, "zr_adamw_shard_step: null hyperparameters");
@@ -355,6 +359,7 @@ extern "C" zr_status zr_adamw_shard_step(const float* shard_sums, float* m, floa
 
 extern "C" zr_status zr_all_gather(const float* master, int64_t n, zr_dtype out_dt, void* const* replicas,
                                    int n_replicas, void* stream) {
+  zr::Range range("zr_all_gather");
   zr::clear_error();
   if (n < 0) return fail(ZR_ERR_INVALID, "zr_all_gather: n < 0");
   if (out_dt != ZR_F16 && out_dt != ZR_BF16) return fail(ZR_ERR_INVALID, "zr_all_gather: dtype must be F16 or BF16");

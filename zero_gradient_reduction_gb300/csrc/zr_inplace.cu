@@ -11,6 +11,7 @@
 
 #include "zr_device.cuh"
 #include "zr_internal.h"
+#include "zr_nvtx.h"
 
 using zr::fail;
 
@@ -33,6 +34,7 @@ zr_status zr::init_inplace(zr_plan* p) {
 
 extern "C" zr_status zr_step_inplace(zr_plan* p, int stage, const void* const* grads, const zr_state1* st,
                                      const zr_adamw_hyper* h, void* stream, zr_step_report* rep) {
+  zr::Range range("zr_step_inplace");
   zr::clear_error();
   if (!p || !st || !h || !grads) return fail(ZR_ERR_INVALID, "zr_step_inplace: null argument");
   if (stage < 1 || stage > 3) return fail(ZR_ERR_INVALID, "zr_step_inplace: stage=%d not in 1..3", stage);

@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "zr_internal.h"
+#include "zr_nvtx.h"
 #include "zr_plan.h"
 
 using zr::fail;
@@ -27,6 +28,7 @@ extern "C" zr_status zr_offload_step(zr_plan* p, int stage, const void* const* g
                                      float* master, float* m, float* v, void* param_host, void* param_dev,
                                      const zr_adamw_hyper* h, float loss_scale, int64_t t, int nthreads,
                                      void* stream, int32_t* overflow) {
+  zr::Range range("zr_offload_step");
   zr::clear_error();
   if (!p || !grads || !sums_dev || !sums_host || !master || !m || !v || !param_host || !param_dev || !h || !overflow)
     return fail(ZR_ERR_INVALID, "zr_offload_step: null argument");

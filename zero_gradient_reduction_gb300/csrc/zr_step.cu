@@ -19,6 +19,7 @@
 
 #include "zr_device.cuh"
 #include "zr_internal.h"
+#include "zr_nvtx.h"
 
 using zr::fail;
 
@@ -318,6 +319,7 @@ static zr_status launch_step(zr_plan* p, int stage, const void* const* grads, co
 
 extern "C" zr_status zr_step(zr_plan* p, int stage, const void* const* grads, const zr_state* st,
                              const zr_adamw_hyper* h, void* stream, zr_step_report* rep) {
+  zr::Range range("zr_step");
   zr::clear_error();
   zr_status s = check_step_args(p, stage, grads, st, h);
   if (s != ZR_OK) return s;
@@ -329,6 +331,7 @@ extern "C" zr_status zr_step(zr_plan* p, int stage, const void* const* grads, co
 
 extern "C" zr_status zr_step_bucket(zr_plan* p, int stage, int bucket, const void* const* grads, const zr_state* st,
                                     const zr_adamw_hyper* h, void* stream) {
+  zr::Range range("zr_step_bucket");
   zr::clear_error();
   zr_status s = check_step_args(p, stage, grads, st, h);
   if (s != ZR_OK) return s;
@@ -341,6 +344,7 @@ extern "C" zr_status zr_step_bucket(zr_plan* p, int stage, int bucket, const voi
 extern "C" zr_status zr_step_from_host(zr_plan* p, int stage, const void* const* host_grads, void* const* dev_grads,
                                        const zr_state* st, const zr_adamw_hyper* h, void* stream,
                                        zr_step_report* rep) {
+  zr::Range range("zr_step_from_host");
   zr::clear_error();
   if (!p || !host_grads || !dev_grads || !rep) return fail(ZR_ERR_INVALID, "zr_step_from_host: null argument");
   const int R = p->W * p->A;

@@ -12,6 +12,7 @@
 
 #include "zr_device.cuh"
 #include "zr_internal.h"
+#include "zr_nvtx.h"
 #include "zr_plan.h"
 
 using zr::fail;
@@ -157,6 +158,7 @@ extern "C" zr_status zr_plan_shard_offset(const zr_plan* p, int bucket, int work
 }
 
 extern "C" zr_status zr_shard_params(zr_plan* p, const void* replica, void* const* shards, void* stream) {
+  zr::Range range("zr_shard_params");
   zr::clear_error();
   zr_status s = check_shards(p, const_cast<const void* const*>(shards), replica, "zr_shard_params");
   if (s != ZR_OK) return s;
@@ -165,6 +167,7 @@ extern "C" zr_status zr_shard_params(zr_plan* p, const void* replica, void* cons
 
 extern "C" zr_status zr_gather_params(zr_plan* p, int bucket_lo, int bucket_hi, const void* const* shards,
                                       void* replica, void* stream) {
+  zr::Range range("zr_gather_params");
   zr::clear_error();
   zr_status s = check_shards(p, shards, replica, "zr_gather_params");
   if (s != ZR_OK) return s;
