@@ -33,4 +33,13 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) % 16 == 0, "Ctrl is read and written as 16-byte words");
 
+// The host AdamW of ZeRO-Offload (zr_offload_host.cpp): its constants for one step, and
+// the update plus 16-bit cast of elements [lo, hi), for callers that run their own threads.
+struct OffloadConsts {
+  float b1, b2, omb1, omb2, lr, eps, decay, bc1, bc2, r;
+};
+OffloadConsts offload_consts(const zr_adamw_hyper& h, float loss_scale, int W, int64_t t);
+void offload_update(const float* sums, float* master, float* m, float* v, void* param16, zr_dtype dt, int64_t lo,
+                    int64_t hi, const OffloadConsts& k);
+
 }  // namespace zr

@@ -2,12 +2,16 @@
 // host CPU. The fp32 master/m/v live in host memory; the reduced gradients go down
 // to the host (4 bytes/param over the host link), the CPU runs the owner-side AdamW
 // (zr_offload_adamw), and the updated 16-bit parameters come back (2 bytes/param).
-// Buckets are pipelined: bucket b's sums are copied down while the CPU updates
-// bucket b-1 and bucket b-2's parameters are copied up.
+// Buckets are pipelined: later buckets' sums are copied down while the CPU updates
+// bucket b, and earlier buckets' parameters are copied up on a second stream.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <memory>
+#include <thread>
 #include <vector>
 
 #include "zr_internal.h"
@@ -59,32 +63,64 @@ extern "C" zr_status zr_offload_step(zr_plan* p, int stage, const void* const* g
     *overflow = 1;
     return ZR_OK;
   }
-  // 3. pipeline per bucket: copy sums down (event), update on the CPU, copy params up
+  // 3. pipeline per bucket. Every bucket's sums are queued down on `stream`, each followed
+  //    by an event. A team of nthreads host threads walks the buckets in order: each waits
+  //    for a bucket's event and updates its slice of the bucket (AdamW and the cast in one
+  //    pass), and the last thread to finish the bucket queues its parameters up on a second
+  //    stream, so that copies up overlap copies down and the host never waits for them.
   const size_t nb = p->buckets.size();
+  cudaStream_t up = nullptr;
   std::vector<cudaEvent_t> down(nb, nullptr);
+  cudaEvent_t up_done = nullptr;
+  e = cudaStreamCreateWithFlags(&up, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&up_done, cudaEventDisableTiming);
   for (size_t b = 0; b < nb && e == cudaSuccess; ++b) e = cudaEventCreateWithFlags(&down[b], cudaEventDisableTiming);
   for (size_t b = 0; b < nb && e == cudaSuccess; ++b) {
     const zr_bucket& bk = p->buckets[b];
     e = cudaMemcpyAsync(sums_host + bk.start, sums_dev + bk.start, (size_t)bk.len * 4, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaEventRecord(down[b], s);
   }
-  zr_status st = ZR_OK;
-  for (size_t b = 0; b < nb && e == cudaSuccess && st == ZR_OK; ++b) {
-    const zr_bucket& bk = p->buckets[b];
-    e = cudaEventSynchronize(down[b]);
-    if (e != cudaSuccess) break;
-    int32_t of = 0;
-    st = zr_offload_adamw(sums_host + bk.start, master + bk.start, m + bk.start, v + bk.start,
-                          static_cast<char*>(param_host) + (size_t)bk.start * 2, p->dtype, bk.len, h, loss_scale,
-                          p->W, t, nthreads, &of);
-    if (st == ZR_OK)
-      e = cudaMemcpyAsync(static_cast<char*>(param_dev) + (size_t)bk.start * 2,
-                          static_cast<const char*>(param_host) + (size_t)bk.start * 2, (size_t)bk.len * 2,
-                          cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) {
+    const zr::OffloadConsts k = zr::offload_consts(*h, loss_scale, p->W, t);
+    const int nt = nthreads < 1 ? 1 : (nthreads > 256 ? 256 : nthreads);
+    std::unique_ptr<std::atomic<int>[]> left(new std::atomic<int>[nb]);
+    for (size_t b = 0; b < nb; ++b) left[b].store(nt);
+    std::atomic<int> err{(int)cudaSuccess};
+    auto note = [&](cudaError_t ee) {
+      int ok = (int)cudaSuccess;
+      if (ee != cudaSuccess) err.compare_exchange_strong(ok, (int)ee);
+    };
+    auto work = [&](int tid) {
+      for (size_t b = 0; b < nb; ++b) {
+        const zr_bucket& bk = p->buckets[b];
+        if (err.load() == (int)cudaSuccess) {
+          const cudaError_t ee = cudaEventSynchronize(down[b]);
+          note(ee);
+          if (ee == cudaSuccess) {
+            const int64_t per = (bk.len + nt - 1) / nt;
+            const int64_t lo = std::min(per * tid, bk.len), hi = std::min(per * (tid + 1), bk.len);
+            zr::offload_update(sums_host, master, m, v, param_host, p->dtype, bk.start + lo, bk.start + hi, k);
+          }
+        }
+        if (left[b].fetch_sub(1) == 1 && err.load() == (int)cudaSuccess)
+          note(cudaMemcpyAsync(static_cast<char*>(param_dev) + (size_t)bk.start * 2,
+                               static_cast<const char*>(param_host) + (size_t)bk.start * 2, (size_t)bk.len * 2,
+                               cudaMemcpyHostToDevice, up));
+      }
+    };
+    std::vector<std::thread> team;
+    for (int i = 1; i < nt; ++i) team.emplace_back(work, i);
+    work(0);
+    for (auto& th : team) th.join();
+    e = (cudaError_t)err.load();
+    // the caller's stream sees the parameters once every copy up is done
+    if (e == cudaSuccess) e = cudaEventRecord(up_done, up);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, up_done, 0);
   }
   for (cudaEvent_t ev : down)
     if (ev) cudaEventDestroy(ev);
-  if (st != ZR_OK) return st;
+  if (up_done) cudaEventDestroy(up_done);
+  if (up) cudaStreamDestroy(up);
   if (e != cudaSuccess) return cuda_err("pipeline", e);
   *overflow = 0;
   return ZR_OK;

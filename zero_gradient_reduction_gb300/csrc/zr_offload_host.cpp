@@ -48,12 +48,14 @@ uint16_t to_f16(float f) {
   return (uint16_t)(sign | r);
 }
 
-struct Consts {
-  float b1, b2, omb1, omb2, lr, eps, decay, bc1, bc2, r;
-};
+using Consts = zr::OffloadConsts;
 
-void update_slice(const float* __restrict__ sums, float* __restrict__ p, float* __restrict__ m,
-                  float* __restrict__ v, uint16_t* __restrict__ out, int64_t lo, int64_t hi, const Consts k, bool bf16) {
+// AdamW and the cast over elements [lo, hi), in chunks small enough that the cast reads
+// the chunk's fresh master values from cache: one pass over host memory, and each loop
+// simple enough to vectorise.
+void update_chunk(const float* __restrict__ sums, float* __restrict__ p, float* __restrict__ m,
+                  float* __restrict__ v, uint16_t* __restrict__ out, int64_t lo, int64_t hi, const Consts& k,
+                  bool bf16) {
   for (int64_t i = lo; i < hi; ++i) {
     const float g = sums[i] * k.r;
     const float mi = k.b1 * m[i] + k.omb1 * g;
@@ -73,6 +75,12 @@ void update_slice(const float* __restrict__ sums, float* __restrict__ p, float* 
     else
       for (int64_t i = lo; i < hi; ++i) out[i] = to_f16(p[i]);
   }
+}
+
+void update_slice(const float* sums, float* p, float* m, float* v, uint16_t* out, int64_t lo, int64_t hi,
+                  const Consts& k, bool bf16) {
+  constexpr int64_t kChunk = 4096;
+  for (int64_t c = lo; c < hi; c += kChunk) update_chunk(sums, p, m, v, out, c, c + kChunk < hi ? c + kChunk : hi, k, bf16);
 }
 
 bool any_nonfinite(const float* x, int64_t lo, int64_t hi) {
@@ -101,7 +109,28 @@ void parallel_for(int64_t n, int nthreads, F fn) {
 
 namespace zr {
 float bias_correction_host(float beta, int64_t t);
+
+OffloadConsts offload_consts(const zr_adamw_hyper& h, float loss_scale, int W, int64_t t) {
+  OffloadConsts k;
+  k.b1 = h.beta1;
+  k.b2 = h.beta2;
+  k.omb1 = 1.0f - h.beta1;
+  k.omb2 = 1.0f - h.beta2;
+  k.lr = h.lr;
+  k.eps = h.eps;
+  const float lrwd = h.lr * h.weight_decay;
+  k.decay = 1.0f - lrwd;
+  k.bc1 = bias_correction_host(h.beta1, t);
+  k.bc2 = bias_correction_host(h.beta2, t);
+  k.r = (float)(1.0 / ((double)loss_scale * (double)W));
+  return k;
 }
+
+void offload_update(const float* sums, float* master, float* m, float* v, void* param16, zr_dtype dt, int64_t lo,
+                    int64_t hi, const OffloadConsts& k) {
+  update_slice(sums, master, m, v, static_cast<uint16_t*>(param16), lo, hi, k, dt == ZR_BF16);
+}
+}  // namespace zr
 
 extern "C" zr_status zr_offload_adamw(const float* sums, float* master, float* m, float* v, void* param16,
                                       zr_dtype dt, int64_t n, const zr_adamw_hyper* h, float loss_scale, int W,
@@ -122,18 +151,7 @@ extern "C" zr_status zr_offload_adamw(const float* sums, float* master, float* m
       return ZR_OK;  // skipped: nothing written
     }
   *overflow = 0;
-  Consts k;
-  k.b1 = h->beta1;
-  k.b2 = h->beta2;
-  k.omb1 = 1.0f - h->beta1;
-  k.omb2 = 1.0f - h->beta2;
-  k.lr = h->lr;
-  k.eps = h->eps;
-  const float lrwd = h->lr * h->weight_decay;
-  k.decay = 1.0f - lrwd;
-  k.bc1 = zr::bias_correction_host(h->beta1, t);
-  k.bc2 = zr::bias_correction_host(h->beta2, t);
-  k.r = (float)(1.0 / ((double)loss_scale * (double)W));
+  const Consts k = zr::offload_consts(*h, loss_scale, W, t);
   uint16_t* out = static_cast<uint16_t*>(param16);
   const bool bf16 = dt == ZR_BF16;
   parallel_for(n, nthreads, [&](int64_t lo, int64_t hi, int) { update_slice(sums, master, m, v, out, lo, hi, k, bf16); });
