@@ -94,6 +94,8 @@ def lib():
             L.zro_ring_reduce_scatter.restype = None
             L.zro_ring_all_gather.argtypes = [ctypes.c_int, i64, i64, vp, vp, vp, vp]
             L.zro_ring_all_gather.restype = None
+            L.zro_ring_all_reduce.argtypes = [ctypes.c_int, i64, i64, vp, vp, vp, vp]
+            L.zro_ring_all_reduce.restype = None
             L.zro_ring_reduce_scatter_hops.argtypes = [ctypes.c_int, i64, i64, vp, vp, vp, vp, ctypes.c_int,
                                                        ctypes.c_int]
             L.zro_ring_reduce_scatter_hops.restype = None
@@ -207,6 +209,21 @@ def ring_all_gather(reps: List[np.ndarray], C: int, hops: Optional[range] = None
     else:
         lib().zro_ring_all_gather_hops(W, n, int(C), ctypes.addressof(ptrs), _ptr(msg), _ptr(sent), _ptr(recv),
                                        hops.start, hops.stop)
+    return sent, recv
+
+
+def ring_all_reduce(work: List[np.ndarray], C: int):
+    """In place on the W fp32 position arrays (reduce-scatter hops, then all-gather hops of the reduced
+    blocks); returns (sent, recv) element counts per position over both phases."""
+    W = len(work)
+    n = work[0].size
+    for w in work:
+        assert w.dtype == np.float32 and w.size == n
+    ptrs = (ctypes.c_void_p * W)(*[_ptr(w) for w in work])
+    msg = np.empty(max(W * C, 1), dtype=np.float32)
+    sent = np.zeros(W, dtype=np.int64)
+    recv = np.zeros(W, dtype=np.int64)
+    lib().zro_ring_all_reduce(W, n, int(C), ctypes.addressof(ptrs), _ptr(msg), _ptr(sent), _ptr(recv))
     return sent, recv
 
 

@@ -223,6 +223,33 @@ void zro_ring_all_gather(int W, int64_t n, int64_t C, uint16_t* const* rep, uint
     zro_ring_all_gather_hops(W, n, C, rep, msg, sent, recv, 0, W - 1);
 }
 
+/* Ring all-reduce, as DDP runs it on the gradients ([P1] 二: after the scatter-reduce
+ * hops comes the all-gather phase, at the end of which every GPU holds every reduced
+ * block; [P3] Ring AllReduce = ReduceScatter + AllGather). work[p] as in
+ * zro_ring_reduce_scatter; the reduce-scatter hops run first, then in all-gather hop
+ * s = 0..W-2 every position p sends its copy of block (p + 1 - s) mod W, already fully
+ * reduced, to p+1, which stores it. Afterwards every work[p] holds every block's sum.
+ * msg: scratch of W*C floats; sent/recv count both phases. */
+void zro_ring_all_reduce(int W, int64_t n, int64_t C, float* const* work, float* msg,
+                         int64_t* sent, int64_t* recv) {
+    zro_ring_reduce_scatter_hops(W, n, C, work, msg, sent, recv, 0, W - 1);
+    for (int s = 0; s <= W - 2; ++s) {
+        for (int p = 0; p < W; ++p) {
+            int c = mod(p + 1 - s, W);
+            int64_t lo = chunk_lo(n, C, c), hi = chunk_hi(n, C, c);
+            memcpy(msg + (int64_t)p * C, work[p] + lo, (size_t)(hi - lo) * sizeof(float));
+            sent[p] += hi - lo;
+        }
+        for (int p = 0; p < W; ++p) {
+            int dst = mod(p + 1, W);
+            int c = mod(p + 1 - s, W);
+            int64_t lo = chunk_lo(n, C, c), hi = chunk_hi(n, C, c);
+            memcpy(work[dst] + lo, msg + (int64_t)p * C, (size_t)(hi - lo) * sizeof(float));
+            recv[dst] += hi - lo;
+        }
+    }
+}
+
 /* ZeRO-3 keeps on each worker only its share of the 16-bit parameters ([P1] 四:
  * parameters are partitioned too; [P3] ZeRO Stage 3: each GPU stores 1/W of them).
  * Reading: the worker at ring position p keeps the block it owns after the

@@ -100,6 +100,8 @@ void zro_ring_all_gather_hops(int W, int64_t n, int64_t C, uint16_t* const* rep,
                               int64_t* sent, int64_t* recv, int s0, int s1);
 void zro_ring_all_gather(int W, int64_t n, int64_t C, uint16_t* const* rep, uint16_t* msg,
                          int64_t* sent, int64_t* recv);
+void zro_ring_all_reduce(int W, int64_t n, int64_t C, float* const* work, float* msg,
+                         int64_t* sent, int64_t* recv);
 void zro_ring_traffic(int64_t n, int W, int align, int64_t* sent_per_pos, int64_t* recv_per_pos);
 
 /* ---- ZeRO-3 parameter shards and the all-gather before forward/backward ---- */

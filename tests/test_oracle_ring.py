@@ -80,6 +80,53 @@ def test_abc_all_gather_hops():
         assert list(reps[p]) == [11, 22, 33]
 
 
+def test_abc_all_reduce_every_gpu_holds_every_total():
+    """After the scatter reduce and the all-gather every GPU holds the totals of A, B and C (section 二:
+    at the end of the all-gather phase all GPUs have all reduced gradients)."""
+    rows = read_golden("ring_abc_3gpu.txt")
+    totals = {}
+    for phase, _, gpu, blk, contents in rows:
+        if phase == "own":
+            totals[BLOCK[blk]] = sum(_abc_value(t) for t in contents.split("+"))
+    work = _abc_work()
+    sent, recv = oracle.ring_all_reduce(work, 1)
+    for p in range(3):
+        assert [float(x) for x in work[p]] == [totals[0], totals[1], totals[2]]
+    # two phases of W-1 = 2 one-element transfers per GPU
+    assert list(sent) == [4, 4, 4] and list(recv) == [4, 4, 4]
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 8, 9])
+def test_all_reduce_is_the_reduce_scatter_on_every_worker(W):
+    """Brute force: every position ends with every block's left fold in ring order (the reduce-scatter's
+    owner values), bit for bit; traffic 2 (W-1) n / W per position when W divides n into 8-aligned blocks."""
+    rng = np.random.default_rng(300 + W)
+    for trial in range(5):
+        n = 8 * W * int(rng.integers(1, 4)) if trial % 2 == 0 else int(rng.integers(1, 65))
+        C = oracle.chunk_size(n, W, 8)
+        xs = [rng.normal(scale=2.0, size=n).astype(np.float32) for _ in range(W)]
+        order = list(rng.permutation(W))
+        work = [xs[order[p]].copy() for p in range(W)]
+        sent, recv = oracle.ring_all_reduce(work, C)
+        want = _left_fold(xs, order, C, n)
+        for p in range(W):
+            assert np.array_equal(work[p].view(np.uint32), want.view(np.uint32)), (W, n, p)
+        if n % (8 * W) == 0:
+            assert all(int(x) == 2 * (W - 1) * n // W for x in sent)
+            assert all(int(x) == 2 * (W - 1) * n // W for x in recv)
+
+
+def test_all_reduce_integer_gradients_exact():
+    rng = np.random.default_rng(11)
+    W, n = 6, 96
+    ints = [rng.integers(-50, 50, size=n) for _ in range(W)]
+    work = [x.astype(np.float32) for x in ints]
+    oracle.ring_all_reduce(work, oracle.chunk_size(n, W, 8))
+    exact = np.sum(np.stack(ints), axis=0).astype(np.float32)
+    for p in range(W):
+        assert np.array_equal(work[p], exact)
+
+
 @pytest.mark.parametrize("W", [2, 3, 4, 5, 7, 8, 9, 16])
 def test_traffic_per_phase(W):
     rng = np.random.default_rng(W)
