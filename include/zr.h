@@ -121,6 +121,19 @@ zr_status zr_bucket_plan(const int64_t* numels, int ntensors, int64_t cap_elems,
 zr_status zr_reduce_scatter(const void* const* grads, zr_dtype dt, int64_t n, int W, const int* order,
                             float* sums, int32_t* overflow, void* stream);
 
+/* Ring all-reduce of one n-element bucket over W workers, as DDP runs it on the
+ * gradients ([P1] 二: the scatter reduce, then the all-gather phase, after which every
+ * GPU holds every reduced block; [P3] Ring AllReduce = ReduceScatter + AllGather). Every
+ * worker ends with the sums zr_reduce_scatter defines, so the W copies are identical:
+ * out[R] is a host array of R device fp32[n] outputs (the workers' copies; R in
+ * [1, ZR_MAX_REPLICAS], typically 1..W), each written in full. The all-gather hops add
+ * nothing: their traffic is zr_ring_traffic's second phase, counted, not moved.
+ * grads, dt, n, W, order, overflow: as zr_reduce_scatter.
+ * Errors: as zr_reduce_scatter, plus R outside [1, ZR_MAX_REPLICAS] and null or
+ * misaligned outputs. n == 0 is a no-op. */
+zr_status zr_all_reduce(const void* const* grads, zr_dtype dt, int64_t n, int W, const int* order,
+                        float* const* out, int R, int32_t* overflow, void* stream);
+
 /* One micro-batch of gradient accumulation on one worker ([P3] Gradient Accumulation:
  * micro-batch gradients add up locally, with the synchronisation skipped, before the
  * one reduction of the step): acc[i] = fp32(grad[i]) if `first`, else
@@ -167,7 +180,7 @@ typedef struct {
     int32_t W;                /* workers, 1..ZR_MAX_W */
     int32_t A;                /* micro-batches per worker, W*A <= ZR_MAX_REPLICAS */
     zr_dtype dtype;           /* gradient and parameter type: ZR_F16 or ZR_BF16 */
-    int32_t stage;            /* ZeRO stage 1, 2 or 3 (memory plan; same arithmetic) */
+    int32_t stage;            /* 0 = DDP, or ZeRO stage 1, 2 or 3 (memory plan; same arithmetic) */
     int32_t align;            /* tensor alignment in elements; must be ZR_ALIGN */
     int64_t cap;              /* bucket cap in elements */
     int32_t ntensors;
@@ -226,12 +239,15 @@ zr_status zr_plan_reset(zr_plan* p, void* stream);
  * zr_reduce_scatter + zr_adamw_shard_step + zr_all_gather, reading state set k and
  * writing set 1-k. The last block to finish ORs all flags and applies the loss-scale
  * rule; on a clean step it sets t += 1 and k = 1-k ([P2] 核心技术 (3) dynamic scaling).
- * stage must be 1, 2 or 3 ([P3] ZeRO stages; [P2] (11)-(13)): the stages share this
- * arithmetic and differ in what a real worker keeps resident.
+ * stage is 0, 1, 2 or 3 ([P3] ZeRO stages; [P2] (11)-(13)): stage 0 is DDP ([P1] 二:
+ * the gradients are ring-all-reduced and every worker runs the same update on the full
+ * gradient and keeps everything), stages 1-3 shard the optimizer state, the gradients
+ * and the parameters. They share this arithmetic (every worker's update of an element
+ * gives the owner's bits) and differ in what a real worker keeps resident.
  * grads[W*A]: host array of device pointers; replica w*A + a is worker w's micro-batch
  * a, zr_plan_numel elements of the plan's dtype. rep: NULL for a fully asynchronous
  * call; otherwise the call synchronises `stream` and fills *rep.
- * Errors: ZR_ERR_INVALID for a null plan/state/hyper, stage outside 1..3, null or
+ * Errors: ZR_ERR_INVALID for a null plan/state/hyper, stage outside 0..3, null or
  * misaligned pointers, aliasing of the two state sets; ZR_ERR_CUDA. */
 zr_status zr_step(zr_plan* p, int stage, const void* const* grads, const zr_state* st,
                   const zr_adamw_hyper* h, void* stream, zr_step_report* rep);
@@ -286,7 +302,7 @@ typedef struct {
  * bucket-by-bucket form (zr_step_bucket): no bucket may be updated before the flag of
  * the last one is known.
  * rep: NULL for an asynchronous call, else the call synchronises `stream` and fills it.
- * Errors: ZR_ERR_INVALID for a null plan/state/hyper/grads, stage outside 1..3, a null or
+ * Errors: ZR_ERR_INVALID for a null plan/state/hyper/grads, stage outside 0..3, a null or
  * misaligned array; ZR_ERR_CUDA. */
 zr_status zr_step_inplace(zr_plan* p, int stage, const void* const* grads, const zr_state1* st,
                           const zr_adamw_hyper* h, void* stream, zr_step_report* rep);

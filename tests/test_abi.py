@@ -111,9 +111,10 @@ def test_argument_checks_without_gpu(zr):
     assert L.zr_all_gather(16, 8, 2, ctypes.addressof(one), 1, None) == 1  # F32 output not allowed
     assert L.zr_all_gather(16, 8, 1, ctypes.addressof(one), 0, None) == 1
     d = zr.PlanDesc()
-    d.W, d.A, d.dtype, d.stage, d.align, d.cap, d.ntensors = 2, 1, 1, 0, 8, 100, 0
+    d.W, d.A, d.dtype, d.stage, d.align, d.cap, d.ntensors = 2, 1, 1, 4, 8, 100, 0
     out = ctypes.c_void_p()
-    assert L.zr_plan_create(ctypes.byref(d), ctypes.byref(out)) == 1  # stage 0
+    assert L.zr_plan_create(ctypes.byref(d), ctypes.byref(out)) == 1  # stage 4
+    assert b"stage" in L.zr_last_error()
     assert L.zr_model_state_bytes(9, 10, 1) == -1
     s1 = zr.StateC1(16, 16, 16, 16)
     assert L.zr_step_inplace(None, 2, ctypes.addressof(one), ctypes.byref(s1), ctypes.byref(h), None, None) == 1

@@ -71,6 +71,8 @@ def test_guards_standalone_calls():
         flag = Guarded(1, torch.int32)
         flag.t.zero_()
         zr.reduce_scatter([g.t for g in gs], sums.t, flag.t)
+        ar = [Guarded(n, torch.float32) for _ in range(2)]
+        zr.all_reduce([g.t for g in gs], [x.t for x in ar], flag.t)
         m, v, p = (Guarded(n, torch.float32) for _ in range(3))
         m.t.zero_(); v.t.zero_(); p.t.fill_(0.5)
         zr.adamw_shard_step(sums.t, m.t, v.t, p.t, HYPER, 1.0, W, 1, flag.t)
@@ -80,7 +82,7 @@ def test_guards_standalone_calls():
         zr.accumulate(gs[0].t, acc.t, True)
         zr.accumulate(gs[1].t, acc.t, False)
         torch.cuda.synchronize()
-        assert all(x.intact() for x in gs + [sums, flag, m, v, p, acc] + reps), n
+        assert all(x.intact() for x in gs + [sums, flag, m, v, p, acc] + reps + ar), n
 
 
 def test_guards_zero3_and_noalloc():

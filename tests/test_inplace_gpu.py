@@ -130,7 +130,7 @@ def test_inplace_error_paths():
     s1 = plan.new_state1()
     grads = [torch.zeros(plan.numel, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     with pytest.raises(zr.ZrError) as e:
-        plan.step_inplace(grads, s1, HYPER, stage=0)
+        plan.step_inplace(grads, s1, HYPER, stage=4)
     assert e.value.status == 1
     with pytest.raises(zr.ZrError):
         plan.step_inplace([grads[0], grads[1][1:]], s1, HYPER)  # 2-byte offset: misaligned

@@ -125,6 +125,40 @@ def test_reduce_scatter_bit_exact(W, dtype):
         assert int(of.item()) == flag == 0
 
 
+@pytest.mark.parametrize("W", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("dtype", [zr.F16, zr.BF16])
+def test_all_reduce_bit_exact(W, dtype):
+    """Every one of the R outputs equals what the oracle's hop-by-hop all-reduce leaves on every worker."""
+    rng = np.random.default_rng(W * 17 + dtype)
+    for n in (1, 9, 8 * W * 2 + 5, 70_003):
+        order = list(rng.permutation(W))
+        grads = _rand_grads(rng, W, n, dtype)
+        xs = [oracle.decode(dtype, g) for g in grads]
+        work = [xs[order[p]].copy() for p in range(W)]
+        oracle.ring_all_reduce(work, oracle.chunk_size(n, W, 8))
+        for p in range(1, W):
+            assert np.array_equal(work[p].view(np.uint32), work[0].view(np.uint32))
+        outs = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(W)]
+        of = torch.zeros(1, dtype=torch.int32, device="cuda")
+        zr.all_reduce([to_dev16(g, dtype) for g in grads], outs, of, order=order)
+        torch.cuda.synchronize()
+        for o in outs:
+            assert np.array_equal(f32bits(o), work[0].view(np.uint32)), (W, n)
+        assert int(of.item()) == 0
+    # a non-finite input sets the flag; R = 1 is the reduce-scatter
+    grads = _rand_grads(rng, W, 4096, dtype)
+    grads[W - 1][100] = 0x7C00 if dtype == zr.F16 else 0x7F80
+    gd = [to_dev16(g, dtype) for g in grads]
+    one = torch.empty(4096, dtype=torch.float32, device="cuda")
+    rs = torch.empty(4096, dtype=torch.float32, device="cuda")
+    of1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    of2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    zr.all_reduce(gd, [one], of1)
+    zr.reduce_scatter(gd, rs, of2)
+    torch.cuda.synchronize()
+    assert int(of1.item()) == int(of2.item()) == 1 and torch.equal(one.view(torch.int32), rs.view(torch.int32))
+
+
 def test_reduce_scatter_overflow_flag_sticky():
     rng = np.random.default_rng(1)
     W, n = 4, 10_000
@@ -326,14 +360,15 @@ def test_fused_scale_growth():
 
 
 def test_stages_identical():
+    """DDP (stage 0) and ZeRO stages 1-3 give the same bytes."""
     outs = []
-    for stage in (1, 2, 3):
+    for stage in (0, 1, 2, 3):
         run = FusedRun([70_000, 5000], 4, 1, zr.BF16, cap=50_000, S=1.0, seed=11, stage=stage)
         for s in (1, 2):
             rep, _ = run.step(s, stage=stage)
             assert rep.stage == stage
         outs.append([x.tobytes() for x in run.live()])
-    assert outs[0] == outs[1] == outs[2]
+    assert outs[0] == outs[1] == outs[2] == outs[3]
 
 
 @pytest.mark.parametrize("pinned", [True, False])
@@ -366,6 +401,8 @@ def test_error_paths():
     with pytest.raises(zr.ZrError) as e:
         plan.step(grads, st, HYPER, stage=4)
     assert e.value.status == 1
+    with pytest.raises(zr.ZrError):
+        plan.step(grads, st, HYPER, stage=-1)
     with pytest.raises(zr.ZrError):
         plan.step([grads[0], grads[1][1:]], st, HYPER)  # 2-byte offset: misaligned
     st.master[1] = st.master[0]

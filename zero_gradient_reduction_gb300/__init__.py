@@ -95,6 +95,7 @@ def lib():
                 "zr_adamw_shard_step": (st, [vp, vp, vp, vp, i64, ctypes.POINTER(Hyper), ctypes.c_float, i32, i64,
                                              vp, vp]),
                 "zr_all_gather": (st, [vp, i64, i32, vp, i32, vp]),
+                "zr_all_reduce": (st, [vp, i32, i64, i32, vp, vp, i32, vp, vp]),
                 "zr_accumulate": (st, [vp, i32, vp, i64, i32, vp]),
                 "zr_step_bucket": (st, [vp, i32, i32, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp]),
                 "zr_offload_adamw": (st, [vp, vp, vp, vp, vp, i32, i64, ctypes.POINTER(Hyper), ctypes.c_float, i32,
@@ -217,6 +218,19 @@ def reduce_scatter(grads: Sequence, sums, overflow, order: Optional[Sequence[int
     _check(lib().zr_reduce_scatter(ctypes.addressof(arr), _dt_of(grads[0]), n, W,
                                    ctypes.addressof(ordc) if ordc is not None else None, _ptr(sums), _ptr(overflow),
                                    _stream_handle(stream)))
+
+
+def all_reduce(grads: Sequence, outs: Sequence, overflow, order: Optional[Sequence[int]] = None,
+               n: Optional[int] = None, stream=None) -> None:
+    """Ring all-reduce (zr_all_reduce): the ring sums of the W gradient replicas written to every fp32 output."""
+    W = len(grads)
+    n = int(grads[0].numel()) if n is None else int(n)
+    arr = _ptr_array(grads)
+    out = _ptr_array(outs)
+    o = (ctypes.c_int * W)(*order) if order is not None else None
+    _check(lib().zr_all_reduce(ctypes.addressof(arr), _dt_of(grads[0]), n, W,
+                               ctypes.addressof(o) if o is not None else None, ctypes.addressof(out), len(outs),
+                               _ptr(overflow), _stream_handle(stream)))
 
 
 def adamw_shard_step(shard_sums, m, v, master, hyper: AdamW, loss_scale: float, W: int, t: int, overflow,

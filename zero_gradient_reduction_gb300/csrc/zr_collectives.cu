@@ -58,12 +58,12 @@ __device__ __forceinline__ void block_flag_or(bool mine, int32_t* flag_out) {
 
 // ---------------------------------------------------------------- reduce-scatter
 struct RsArgs {
-  const void* grads[ZR_MAX_W];  // indexed by worker
-  int order[ZR_MAX_W];          // ring position -> worker
-  float* sums;
+  const void* grads[ZR_MAX_W];   // indexed by worker
+  int order[ZR_MAX_W];           // ring position -> worker
+  float* out[ZR_MAX_REPLICAS];   // R copies of the sums: 1 for the reduce-scatter, R for the all-reduce
   int32_t* overflow;
   int64_t n, C;
-  int W;
+  int W, R;
 };
 
 // Ring-order fp32 sum of the W values of element group e (8 elements, or the
@@ -105,8 +105,11 @@ __global__ void __launch_bounds__(kThreads) rs_kernel(const __grid_constant__ Rs
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) bad |= zr::nonfinite(s[j]);
-      zr::st_once_f4(a.sums + e, make_float4(s[0], s[1], s[2], s[3]));
-      zr::st_once_f4(a.sums + e + 4, make_float4(s[4], s[5], s[6], s[7]));
+      const float4 lo = make_float4(s[0], s[1], s[2], s[3]), hi = make_float4(s[4], s[5], s[6], s[7]);
+      for (int r = 0; r < a.R; ++r) {
+        zr::st_once_f4(a.out[r] + e, lo);
+        zr::st_once_f4(a.out[r] + e + 4, hi);
+      }
     } else {
       for (int64_t i = e; i < a.n; ++i) {
         float s = zr::load1<DT>(a.grads[a.order[c]], i);
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(kThreads) rs_kernel(const __grid_constant__ Rs
           s = __fadd_rn(s, zr::load1<DT>(a.grads[a.order[pos]], i));
         }
         bad |= zr::nonfinite(s);
-        a.sums[i] = s;
+        for (int r = 0; r < a.R; ++r) a.out[r][i] = s;
       }
     }
   });
@@ -241,41 +244,62 @@ AdamConsts adam_consts_host(const zr_adamw_hyper& h, float bc1, float bc2) {
 }
 }  // namespace zr
 
-extern "C" zr_status zr_reduce_scatter(const void* const* grads, zr_dtype dt, int64_t n, int W, const int* order,
-                                       float* sums, int32_t* overflow, void* stream) {
-  zr::Range range("zr_reduce_scatter");
-  zr::clear_error();
-  if (n < 0) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: n < 0");
-  if (W < 1 || W > ZR_MAX_W) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: W=%d outside [1, %d]", W, ZR_MAX_W);
+namespace {
+// The ring sums of one bucket written to R outputs: the reduce-scatter (R = 1) and the
+// all-reduce (every worker's copy) share the kernel; `what` names the caller in errors.
+zr_status ring_sums(const char* what, const void* const* grads, zr_dtype dt, int64_t n, int W, const int* order,
+                    float* const* out, int R, int32_t* overflow, void* stream) {
+  if (n < 0) return fail(ZR_ERR_INVALID, "%s: n < 0", what);
+  if (W < 1 || W > ZR_MAX_W) return fail(ZR_ERR_INVALID, "%s: W=%d outside [1, %d]", what, W, ZR_MAX_W);
   if (dt != ZR_F16 && dt != ZR_BF16 && dt != ZR_F32)
-    return fail(ZR_ERR_INVALID, "zr_reduce_scatter: dtype must be F16, BF16 or F32");
-  if (!grads || !sums || !overflow) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: null pointer");
-  if (!zr::aligned16(sums) || (reinterpret_cast<uintptr_t>(overflow) & 3u))
-    return fail(ZR_ERR_INVALID, "zr_reduce_scatter: misaligned output");
+    return fail(ZR_ERR_INVALID, "%s: dtype must be F16, BF16 or F32", what);
+  if (R < 1 || R > ZR_MAX_REPLICAS) return fail(ZR_ERR_INVALID, "%s: R=%d outside [1, %d]", what, R, ZR_MAX_REPLICAS);
+  if (!grads || !out || !overflow) return fail(ZR_ERR_INVALID, "%s: null pointer", what);
+  if (reinterpret_cast<uintptr_t>(overflow) & 3u) return fail(ZR_ERR_INVALID, "%s: misaligned overflow flag", what);
   RsArgs a{};
+  for (int r = 0; r < R; ++r) {
+    if (!out[r] || !zr::aligned16(out[r])) return fail(ZR_ERR_INVALID, "%s: output %d null or misaligned", what, r);
+    a.out[r] = out[r];
+  }
   bool seen[ZR_MAX_W] = {};
   for (int p = 0; p < W; ++p) {
     const int w = order ? order[p] : p;
-    if (w < 0 || w >= W || seen[w]) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: order is not a permutation");
+    if (w < 0 || w >= W || seen[w]) return fail(ZR_ERR_INVALID, "%s: order is not a permutation", what);
     seen[w] = true;
     a.order[p] = w;
   }
   for (int w = 0; w < W; ++w) {
-    if (!grads[w] || !zr::aligned16(grads[w])) return fail(ZR_ERR_INVALID, "zr_reduce_scatter: grads[%d] null or misaligned", w);
+    if (!grads[w] || !zr::aligned16(grads[w])) return fail(ZR_ERR_INVALID, "%s: grads[%d] null or misaligned", what, w);
     a.grads[w] = grads[w];
   }
   if (n == 0) return ZR_OK;
-  a.sums = sums;
   a.overflow = overflow;
   a.n = n;
   a.C = zr_chunk_size(n, W, ZR_ALIGN);
   a.W = W;
+  a.R = R;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int grid = chunk_grid(n);
   if (dt == ZR_F16) launch_rs<zr::DT_F16>(a, grid, s);
   else if (dt == ZR_BF16) launch_rs<zr::DT_BF16>(a, grid, s);
   else launch_rs<zr::DT_F32>(a, grid, s);
-  return launch_status("zr_reduce_scatter");
+  return launch_status(what);
+}
+}  // namespace
+
+extern "C" zr_status zr_reduce_scatter(const void* const* grads, zr_dtype dt, int64_t n, int W, const int* order,
+                                       float* sums, int32_t* overflow, void* stream) {
+  zr::Range range("zr_reduce_scatter");
+  zr::clear_error();
+  float* const out[1] = {sums};
+  return ring_sums("zr_reduce_scatter", grads, dt, n, W, order, out, 1, overflow, stream);
+}
+
+extern "C" zr_status zr_all_reduce(const void* const* grads, zr_dtype dt, int64_t n, int W, const int* order,
+                                   float* const* out, int R, int32_t* overflow, void* stream) {
+  zr::Range range("zr_all_reduce");
+  zr::clear_error();
+  return ring_sums("zr_all_reduce", grads, dt, n, W, order, out, R, overflow, stream);
 }
 
 // ---------------------------------------------------------------- accumulate

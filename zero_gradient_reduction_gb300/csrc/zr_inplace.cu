@@ -37,7 +37,7 @@ extern "C" zr_status zr_step_inplace(zr_plan* p, int stage, const void* const* g
   zr::Range range("zr_step_inplace");
   zr::clear_error();
   if (!p || !st || !h || !grads) return fail(ZR_ERR_INVALID, "zr_step_inplace: null argument");
-  if (stage < 1 || stage > 3) return fail(ZR_ERR_INVALID, "zr_step_inplace: stage=%d not in 1..3", stage);
+  if (stage < 0 || stage > 3) return fail(ZR_ERR_INVALID, "zr_step_inplace: stage=%d not in 0..3", stage);
   for (int r = 0; r < p->W * p->A; ++r)
     if (!grads[r] || !zr::aligned16(grads[r]))
       return fail(ZR_ERR_INVALID, "zr_step_inplace: grads[%d] null or misaligned", r);

@@ -36,7 +36,7 @@ extern "C" zr_status zr_offload_step(zr_plan* p, int stage, const void* const* g
   zr::clear_error();
   if (!p || !grads || !sums_dev || !sums_host || !master || !m || !v || !param_host || !param_dev || !h || !overflow)
     return fail(ZR_ERR_INVALID, "zr_offload_step: null argument");
-  if (stage < 1 || stage > 3) return fail(ZR_ERR_INVALID, "zr_offload_step: stage=%d not in 1..3", stage);
+  if (stage < 0 || stage > 3) return fail(ZR_ERR_INVALID, "zr_offload_step: stage=%d not in 0..3", stage);
   if (p->A != 1) return fail(ZR_ERR_UNSUPPORTED, "zr_offload_step: plans with A > 1 (accumulate first)");
   if (t < 1) return fail(ZR_ERR_INVALID, "zr_offload_step: t must be >= 1");
   if (!zr::aligned16(sums_dev) || !zr::aligned16(param_dev))

@@ -62,7 +62,7 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   if (d->A < 1 || (int64_t)d->W * d->A > ZR_MAX_REPLICAS)
     return fail(ZR_ERR_INVALID, "zr_plan_create: A=%d (W*A must be in [1, %d])", d->A, ZR_MAX_REPLICAS);
   if (d->dtype != ZR_F16 && d->dtype != ZR_BF16) return fail(ZR_ERR_INVALID, "zr_plan_create: dtype must be F16 or BF16");
-  if (d->stage < 1 || d->stage > 3) return fail(ZR_ERR_INVALID, "zr_plan_create: stage=%d not in 1..3", d->stage);
+  if (d->stage < 0 || d->stage > 3) return fail(ZR_ERR_INVALID, "zr_plan_create: stage=%d not in 0..3", d->stage);
   if (d->align != ZR_ALIGN) return fail(ZR_ERR_INVALID, "zr_plan_create: align must be %d", ZR_ALIGN);
   if (d->ntensors < 1 || !d->numels) return fail(ZR_ERR_INVALID, "zr_plan_create: empty tensor list");
   if (d->cap < 1) return fail(ZR_ERR_INVALID, "zr_plan_create: cap < 1");
@@ -290,7 +290,7 @@ extern "C" zr_status zr_plan_restore(zr_plan* p, const zr_checkpoint* in, void* 
 static zr_status check_step_args(const zr_plan* p, int stage, const void* const* grads, const zr_state* st,
                                  const zr_adamw_hyper* h) {
   if (!p || !st || !h || !grads) return fail(ZR_ERR_INVALID, "zr_step: null argument");
-  if (stage < 1 || stage > 3) return fail(ZR_ERR_INVALID, "zr_step: stage=%d not in 1..3", stage);
+  if (stage < 0 || stage > 3) return fail(ZR_ERR_INVALID, "zr_step: stage=%d not in 0..3", stage);
   for (int r = 0; r < p->W * p->A; ++r)
     if (!grads[r] || !zr::aligned16(grads[r])) return fail(ZR_ERR_INVALID, "zr_step: grads[%d] null or misaligned", r);
   for (int k = 0; k < 2; ++k) {
