@@ -234,6 +234,50 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
           }
         }
       }
+    } else if (WT == 0 && AT == 1 && GT == DT) {
+      // Any other W (5-7, 16, 32, 64 ...): the group's state loads, then the replicas in
+      // batches of kBatch whose loads are issued together, added in ring order as they
+      // arrive.
+      constexpr int kBatch = 8;
+      for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+        const int64_t e = start + (int64_t)g * 8;
+        float4 st[6];
+        if constexpr (kState) {
+          st[0] = ld_state<MODE>(mst_in + e);
+          st[1] = ld_state<MODE>(mst_in + e + 4);
+          st[2] = ld_state<MODE>(m_in + e);
+          st[3] = ld_state<MODE>(m_in + e + 4);
+          st[4] = ld_state<MODE>(v_in + e);
+          st[5] = ld_state<MODE>(v_in + e + 4);
+        }
+        float s[8];
+        for (int h0 = 0; h0 < W; h0 += kBatch) {
+          uint4 raw[kBatch];
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) {
+            if (h0 + j < W) {
+              int pos = c + h0 + j;  // c < W and h0 + j < W
+              pos -= pos >= W ? W : 0;
+              raw[j] = zr::ld_once(static_cast<const uint16_t*>(a.grads[a.order[pos]]) + e);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) {
+            if (h0 + j < W) {
+              float x[8];
+              zr::unpack8<DT>(raw[j], x);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) s[k] = h0 + j == 0 ? x[k] : __fadd_rn(s[k], x[k]);
+            }
+          }
+        }
+        if constexpr (kState) {
+          bad |= update_group<DT>(a, K, out, e, s, st[0], st[1], st[2], st[3], st[4], st[5]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) bad |= zr::nonfinite(s[j]);
+        }
+      }
     } else {
       for (int g = threadIdx.x; g < groups; g += blockDim.x) {
         const int64_t off = (int64_t)g * 8, e = start + off;
