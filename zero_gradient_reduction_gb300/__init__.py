@@ -544,5 +544,5 @@ def step_noalloc(buckets: np.ndarray, W: int, A: int, dtype: int, grads: Sequenc
 
 
 __all__ = ["lib", "ZrError", "chunk_size", "bucket_plan", "model_state_bytes", "ring_traffic", "reduce_scatter",
-           "adamw_shard_step", "all_gather", "AdamW", "Scaler", "State", "Plan", "step_noalloc", "F16", "BF16",
-           "F32"]
+           "all_reduce", "adamw_shard_step", "accumulate", "offload_adamw", "all_gather", "AdamW", "Scaler",
+           "State", "State1", "Plan", "step_noalloc", "F16", "BF16", "F32"]
