@@ -116,6 +116,12 @@ def test_argument_checks_without_gpu(zr):
     assert L.zr_plan_create(ctypes.byref(d), ctypes.byref(out)) == 1  # stage 4
     assert b"stage" in L.zr_last_error()
     assert L.zr_model_state_bytes(9, 10, 1) == -1
+    outs = (ctypes.c_void_p * 2)(16, 16)
+    assert L.zr_all_reduce(ctypes.addressof(one), 1, 16, 1, None, ctypes.addressof(outs), 0, 16, None) == 1  # R = 0
+    assert L.zr_all_reduce(ctypes.addressof(one), 1, 16, 0, None, ctypes.addressof(outs), 2, 16, None) == 1  # W = 0
+    bad = (ctypes.c_void_p * 2)(16, 24)
+    assert L.zr_all_reduce(ctypes.addressof(one), 1, 16, 1, None, ctypes.addressof(bad), 2, 16, None) == 1
+    assert b"output 1" in L.zr_last_error()
     s1 = zr.StateC1(16, 16, 16, 16)
     assert L.zr_step_inplace(None, 2, ctypes.addressof(one), ctypes.byref(s1), ctypes.byref(h), None, None) == 1
     assert b"zr_step_inplace" in L.zr_last_error()
