@@ -238,3 +238,32 @@ def test_inplace_fp32_gradients_equal_pingpong(W, A):
             assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), step
     pa.close()
     pb.close()
+
+
+def test_inplace_checkpoint_resume_is_byte_identical():
+    """Four in-place steps straight against two, a checkpoint (control block + the one set), a restore into
+    a fresh plan and two more: the same bytes, with a skip in between."""
+    import oracle
+    numels = [30_000, 5_000, 17_000]
+    kw = dict(cap=25_000, S=65536.0, dynamic=True, seed=9, interval=2)
+    straight = InPlaceRun(numels, 2, 1, zr.F16, **kw)
+    inj = (0, int(straight.plan.tensor_offsets[1]) + 7)
+    for s in range(1, 5):
+        straight.step(s, inject=inj if s == 2 else None)
+    first = InPlaceRun(numels, 2, 1, zr.F16, **kw)
+    for s in (1, 2):
+        first.step(s, inject=inj if s == 2 else None)
+    ck = first.plan.checkpoint()
+    assert ck.t == 1 and ck.skipped == 1 and ck.scale == 32768.0 and ck.current == 0
+    second = InPlaceRun(numels, 2, 1, zr.F16, **kw)
+    second.plan.restore(ck)
+    for name in ("master", "m", "v", "param"):
+        getattr(second.state1, name).copy_(getattr(first.state1, name))
+    second.o = [x.copy() for x in first.o]
+    second.osc = oracle.Scaler.from_buffer_copy(first.osc)
+    second.S = ck.scale
+    for s in (3, 4):
+        second.step(s)
+    for a, b in zip(straight.live(), second.live()):
+        assert a.tobytes() == b.tobytes()
+    second.check("resumed in place: ")

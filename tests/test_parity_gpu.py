@@ -359,6 +359,25 @@ def test_fused_scale_growth():
     run.check()
 
 
+def test_default_growth_interval_over_a_thousand_steps():
+    """The default rule (growth after 1000 clean steps) run to its first growth: the scale doubles on step
+    1001 exactly, a skip at step 1003 halves it and resets the count, and the state after 1005 steps is the
+    oracle's, bit for bit."""
+    run = FusedRun([2048, 1000], 2, 1, zr.F16, cap=4096, S=1024.0, dynamic=True, seed=13, interval=1000)
+    for s in range(1, 1006):
+        rep, _ = run.step(s, inject=(1, 5) if s == 1003 else None)
+        if s <= 1000:
+            assert rep.scale_used == 1024.0
+        if s == 1000:
+            assert rep.scale == 2048.0 and rep.good == 0
+        if s in (1001, 1002, 1003):
+            assert rep.scale_used == 2048.0
+        if s == 1003:
+            assert rep.overflow == 1 and rep.scale == 1024.0 and rep.good == 0
+    assert rep.t == 1004 and rep.steps == 1005 and rep.skipped_total == 1
+    run.check("after 1005 steps: ")
+
+
 def test_stages_identical():
     """DDP (stage 0) and ZeRO stages 1-3 give the same bytes."""
     outs = []
