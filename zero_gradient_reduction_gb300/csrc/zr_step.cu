@@ -164,7 +164,8 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   p->resident = full;
   p->grid = zr::step_grid(p, p->ntiles);
   for (size_t b = 0; b + 1 < p->tile_begin.size(); ++b) {
-    p->bucket_grid.push_back(zr::step_grid(p, p->tile_begin[b + 1] - p->tile_begin[b]));
+    const int64_t nt = p->tile_begin[b + 1] - p->tile_begin[b];
+    p->bucket_grid.push_back(nt > 0 ? zr::step_grid(p, nt) : 0);  // a bucket without tiles launches nothing
     p->bucket_blocks += (unsigned)p->bucket_grid.back();
   }
   if (e == cudaSuccess && !tiles.empty()) e = cudaMalloc(&p->tiles_dev, tiles.size() * sizeof(int4));
