@@ -333,7 +333,7 @@ class State1:
 
 
 class Plan:
-    """A bucketed ZeRO step over W emulated workers (zr_plan_create / zr_step)."""
+    """A bucketed ZeRO step over W emulated workers (zr_plan_create / zr_step); stage 0 is DDP, 1-3 ZeRO."""
 
     def __init__(self, numels: Sequence[int], W: int, A: int = 1, dtype: int = BF16, stage: int = 2,
                  cap: int = 25_000_000, order: Optional[Sequence[int]] = None, scaler: Scaler = Scaler(),
