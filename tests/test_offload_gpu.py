@@ -65,3 +65,44 @@ def test_offload_step_matches_oracle(W, dtype):
             assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
         assert np.array_equal(u16(param_dev), o[3])
     plan.close()
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_offload_random_plans_and_thread_counts(case):
+    """Random layouts, caps and host thread counts (1 to more threads than a bucket has elements per
+    thread): the team's slices of every bucket cover it exactly once and the result is the oracle's."""
+    rng = np.random.default_rng(500 + case)
+    W = int(rng.choice([1, 2, 3, 5, 8]))
+    dtype = int(rng.choice([zr.F16, zr.BF16]))
+    numels = [int(x) for x in rng.choice([0, 1, 9, 1000, 33_333, 100_000], size=int(rng.integers(1, 8)))]
+    if sum(numels) == 0:
+        numels[0] = 500
+    cap = int(rng.choice([8, 1000, 50_000, 1 << 20]))
+    nthreads = int(rng.choice([1, 3, 16, 64]))
+    order = [int(x) for x in rng.permutation(W)]
+    plan = zr.Plan(numels, W=W, dtype=dtype, stage=2, cap=cap, order=order)
+    n = plan.numel
+    tdt = plan.torch_dtype()
+    lay = Layout(numels, plan.tensor_offsets, np.full(len(numels), 1e-2, F32), 40 + case, dtype)
+    table = torch.from_numpy(zrgen.normal_table().copy()).cuda()
+    cs = torch.cuda.current_stream().cuda_stream
+    grads = [torch.zeros(n, dtype=tdt, device="cuda") for _ in range(W)]
+    for r in range(W):
+        lay.grads_dev(grads[r], 1, r, 1.0, table, cs)
+    og = [lay.grads_host(0, n, 1, r, 1.0) for r in range(W)]
+    master = lay.master_host(0, n)
+    m, v = np.zeros(n, F32), np.zeros(n, F32)
+    o = [master.copy(), m.copy(), v.copy(), np.zeros(n, np.uint16)]
+    sums_dev = torch.empty(max(n, 4), dtype=torch.float32, device="cuda")
+    sums_host = torch.empty(max(n, 4), dtype=torch.float32, pin_memory=True)
+    param_host = torch.empty(max(n, 8), dtype=tdt, pin_memory=True)
+    param_dev = torch.zeros(max(n, 8), dtype=tdt, device="cuda")
+    of = plan.offload_step(grads, sums_dev, sums_host, master, m, v, param_host, param_dev, zr.AdamW(), 1.0, 1,
+                           nthreads=nthreads)
+    torch.cuda.synchronize()
+    rep, _ = oracle.step(W, 1, dtype, plan.buckets, og, *o, OHYPER, oracle.new_scaler(1.0), order=order)
+    assert of == rep.overflow == 0
+    for a, b in zip((master, m, v), o[:3]):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (case, W, cap, nthreads)
+    assert np.array_equal(u16(param_dev)[:n], o[3])
+    plan.close()
