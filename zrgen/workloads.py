@@ -97,6 +97,11 @@ WORKLOADS = {
                    sigma=1e-2, init_scale=65536.0, dynamic=True, inject_step=3,
                    description="flat 7.0e9 params in 200M-param buckets, W=2, fp16, dynamic loss scale S0=65536, "
                                "+inf injected at step 3"),
+    # the GPT-2 shapes with A = 4 micro-batches on W = 2 workers: a case small enough (about 6 GB on the
+    # device) for full profiler captures of the accumulate path's kernels
+    "gpt2_a4": Workload("gpt2_a4", tuple(_g2), W=2, A=4, dtype=1, stage=2, cap=25_000_000, steps=3, seed=0,
+                        sigma=None, init_scale=1.0, dynamic=False,
+                        description="GPT-2-small shapes, 123,586,560 params, W=2, A=4, bf16, 25M-param buckets"),
     # a model whose ping-pong state sets do not fit one GPU (1.3e10 x 32 B = 416 GB) but whose in-place step does
     # (1.3e10 x 18 B = 234 GB): the 13B size that ZeRO-Offload is said to train on a single GPU (page
     # "并行训练框架DeepSpeed介绍", (16) ZeRO-Offload), here with all of the optimizer state in HBM
