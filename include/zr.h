@@ -397,7 +397,7 @@ zr_status zr_offload_step(zr_plan* p, int stage, const void* const* grads, float
 /* ------------------------------------------------------------------------- */
 
 /* Tile capacity of the static scratch used by zr_step_noalloc: 16 bytes per tile of at
- * most 8192 elements, i.e. 1 MiB of device memory per GPU, enough for about 5e8
+ * most 32768 elements, i.e. 1 MiB of device memory per GPU, enough for about 2e9
  * elements when the ring blocks are long. */
 #define ZR_NOALLOC_MAX_TILES 65536
 
@@ -408,7 +408,7 @@ zr_status zr_offload_step(zr_plan* p, int stage, const void* const* grads, float
  * would synchronise the device on its path. zr_step_noalloc computes exactly what
  * zr_step computes for one step, allocating nothing (no cudaMalloc, no cudaFree, no
  * allocating library routine): its scratch is one static device array of this library
- * (ZR_NOALLOC_MAX_TILES tiles plus a 256-byte header), present on every GPU that loads
+ * (ZR_NOALLOC_MAX_TILES tiles plus a 256-byte control block), present on every GPU that loads
  * the library until the process exits.
  *
  * buckets[nbuckets]: host bucket table, e.g. from zr_bucket_plan (starts and lengths
