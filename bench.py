@@ -575,13 +575,11 @@ def run_zr(args, w):
         for r in range(w.W * w.A):
             host[r].copy_(grads[r])
         if inplace_main:
-            # one set in place: the pinned host gradients are copied into the device replicas (one
-            # cudaMemcpyAsync each, on the step's stream), then zr_step_inplace reads them twice in HBM
+            # one set in place: the pinned host gradients are copied into the device replicas bucket by
+            # bucket, then the in-place step reads them twice in HBM
             def e2e_step():
-                for r in range(w.W * w.A):
-                    grads[r].copy_(host[r], non_blocking=True)
-                return plan.step_inplace(grads, state, hyper, stream=stream, report=True)
-            api = "pinned host grads copied to the device replicas, zr_step_inplace, report read back"
+                return plan.step_inplace_from_host(host, grads, state, hyper, stream=stream)
+            api = "zr_step_inplace_from_host (pinned host grads copied to the device, in-place step, report read back)"
         else:
             dgr = [torch.empty_like(g) for g in grads]
 

@@ -307,6 +307,17 @@ typedef struct {
 zr_status zr_step_inplace(zr_plan* p, int stage, const void* const* grads, const zr_state1* st,
                           const zr_adamw_hyper* h, void* stream, zr_step_report* rep);
 
+/* As zr_step_inplace, with the gradients in HOST memory, and the report read back (rep
+ * is required): each host_grads[r] is copied into the device buffer dev_grads[r]
+ * (zr_plan_numel elements of the gradient type) with one cudaMemcpyAsync per replica and
+ * bucket, in bucket order, on `stream`, then the in-place step runs on dev_grads. The
+ * gradients always go through device memory here: the step reads them twice (flag pass,
+ * then update), so reading page-locked host memory in place would cross the host link
+ * twice. Errors: as zr_step_inplace, plus null host or device gradient pointers. */
+zr_status zr_step_inplace_from_host(zr_plan* p, int stage, const void* const* host_grads, void* const* dev_grads,
+                                    const zr_state1* st, const zr_adamw_hyper* h, void* stream,
+                                    zr_step_report* rep);
+
 /* Synchronises `stream` and reads the control block into *rep. */
 zr_status zr_plan_report(zr_plan* p, void* stream, zr_step_report* rep);
 

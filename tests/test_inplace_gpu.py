@@ -267,3 +267,23 @@ def test_inplace_checkpoint_resume_is_byte_identical():
     for a, b in zip(straight.live(), second.live()):
         assert a.tobytes() == b.tobytes()
     second.check("resumed in place: ")
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_inplace_from_host_equals_inplace(pinned):
+    """zr_step_inplace_from_host: the host gradients copied in, then the same in-place step."""
+    numels = [50_000, 777, 12_345]
+    a = InPlaceRun(numels, 3, 1, zr.F16, cap=40_000, S=1024.0, seed=2)
+    b = InPlaceRun(numels, 3, 1, zr.F16, cap=40_000, S=1024.0, seed=2)
+    for s in (1, 2):
+        a.step(s)
+        host = []
+        for r in range(3):
+            g = b.layout.grads_host(0, b.n, s, r, b.S)
+            host.append(torch.from_numpy(g.view(np.int16).copy()).pin_memory() if pinned else g.copy())
+        for d in b.grads:
+            d.fill_(0)
+        rep = b.plan.step_inplace_from_host(host, b.grads, b.state1, HYPER)
+        assert rep.t == s and rep.overflow == 0 and rep.current == 0
+        for x, y in zip(a.live(), b.live()):
+            assert x.tobytes() == y.tobytes()

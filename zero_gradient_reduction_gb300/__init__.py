@@ -116,6 +116,8 @@ def lib():
                                  ctypes.POINTER(StepReport)]),
                 "zr_step_inplace": (st, [vp, i32, vp, ctypes.POINTER(StateC1), ctypes.POINTER(Hyper), vp,
                                          ctypes.POINTER(StepReport)]),
+                "zr_step_inplace_from_host": (st, [vp, i32, vp, vp, ctypes.POINTER(StateC1), ctypes.POINTER(Hyper),
+                                                   vp, ctypes.POINTER(StepReport)]),
                 "zr_step_from_host": (st, [vp, i32, vp, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp,
                                            ctypes.POINTER(StepReport)]),
                 "zr_plan_report": (st, [vp, vp, ctypes.POINTER(StepReport)]),
@@ -402,6 +404,19 @@ class Plan:
         _check(lib().zr_step_inplace(self._h, int(stage if stage is not None else self.stage), ctypes.addressof(arr),
                                      ctypes.byref(st), ctypes.byref(h), _stream_handle(stream),
                                      ctypes.byref(rep) if rep is not None else None))
+        return rep
+
+    def step_inplace_from_host(self, host_grads: Sequence, dev_grads: Sequence, state: State1, hyper: AdamW,
+                               stage: Optional[int] = None, stream=None) -> StepReport:
+        """zr_step_inplace_from_host: host gradients copied into dev_grads, then the in-place step; report."""
+        ha = _host_ptr_array(host_grads)
+        da = _ptr_array(dev_grads)
+        st = state.c()
+        h = hyper.c()
+        rep = StepReport()
+        _check(lib().zr_step_inplace_from_host(self._h, int(stage if stage is not None else self.stage),
+                                               ctypes.addressof(ha), ctypes.addressof(da), ctypes.byref(st),
+                                               ctypes.byref(h), _stream_handle(stream), ctypes.byref(rep)))
         return rep
 
     def capture(self, grads: Sequence, state, hyper: AdamW, stage: Optional[int] = None, steps: int = 1):

@@ -66,3 +66,30 @@ extern "C" zr_status zr_step_inplace(zr_plan* p, int stage, const void* const* g
   if (e != cudaSuccess) return fail(ZR_ERR_CUDA, "zr_step_inplace: launch failed: %s", cudaGetErrorString(e));
   return rep ? zr_plan_report(p, stream, rep) : ZR_OK;
 }
+
+extern "C" zr_status zr_step_inplace_from_host(zr_plan* p, int stage, const void* const* host_grads,
+                                               void* const* dev_grads, const zr_state1* st, const zr_adamw_hyper* h,
+                                               void* stream, zr_step_report* rep) {
+  zr::Range range("zr_step_inplace_from_host");
+  zr::clear_error();
+  if (!p || !host_grads || !dev_grads || !rep)
+    return fail(ZR_ERR_INVALID, "zr_step_inplace_from_host: null argument");
+  const int R = p->W * p->A;
+  for (int r = 0; r < R; ++r)
+    if (!host_grads[r] || !dev_grads[r] || !zr::aligned16(dev_grads[r]))
+      return fail(ZR_ERR_INVALID, "zr_step_inplace_from_host: replica %d: null pointer or misaligned device buffer", r);
+  if (!st || !h) return fail(ZR_ERR_INVALID, "zr_step_inplace_from_host: null argument");
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const size_t esz = p->fp32_grads ? 4 : 2;
+  for (const zr_bucket& b : p->buckets) {
+    for (int r = 0; r < R; ++r) {
+      const size_t off = (size_t)b.start * esz, bytes = (size_t)b.len * esz;
+      const cudaError_t e = cudaMemcpyAsync(static_cast<char*>(dev_grads[r]) + off,
+                                            static_cast<const char*>(host_grads[r]) + off, bytes,
+                                            cudaMemcpyHostToDevice, cs);
+      if (e != cudaSuccess)
+        return fail(ZR_ERR_CUDA, "zr_step_inplace_from_host: copy: %s", cudaGetErrorString(e));
+    }
+  }
+  return zr_step_inplace(p, stage, const_cast<const void* const*>(dev_grads), st, h, stream, rep);
+}
