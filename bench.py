@@ -29,7 +29,9 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD_DEFAULT = "1p3b"
+WORKLOAD_DEFAULT = "7b"
+# the other workload held to the HBM target, timed after the default one and reported under its own key
+SECOND_DEFAULT = "1p3b"
 
 
 def _dist_env():
@@ -241,7 +243,8 @@ def _config(w, buckets, l2_note, launch=None, inplace=False):
     return cfg
 
 
-def measure_overlap(torch, zr, plan, grads, state, hyper, dev, stream, tokens: int = 8192, reps: int = 3):
+def measure_overlap(torch, zr, plan, grads, state, hyper, dev, stream, tokens: int = 8192, reps: int = 3,
+                    budget_caps=(16, 38, 76, 152, 304)):
     """Bucketed overlap against a synthetic backward: on a compute stream, bucket b's "backward" is a bf16 GEMM
     of about 4 * tokens * n_b FLOPs (weight and input gradients of n_b parameters), after which an event marks
     the bucket's gradients ready and zr_step_bucket(b) runs on a side stream. Compared with backward followed by
@@ -291,44 +294,61 @@ def measure_overlap(torch, zr, plan, grads, state, hyper, dev, stream, tokens: i
         fn()
     t_bwd, t_step = timed(backward), timed(step_only)
     t_serial, t_over = timed(serial), timed(overlapped)
+    # the same overlap with every bucket launch capped at a block budget (zr_plan_set_bucket_blocks), as a
+    # communication library keeps to a few SMs; 0 = uncapped (one block per tile)
+    budgets = {}
+    for cap in budget_caps:
+        plan.set_bucket_blocks(cap)
+        overlapped()
+        t_cap = timed(overlapped)
+        budgets[str(cap)] = {"overlapped_ms": t_cap,
+                             "hidden_fraction_of_step": (t_serial - t_cap) / t_step if t_step > 0 else None}
+    plan.set_bucket_blocks(0)
     return {"backward_ms": t_bwd, "step_ms": t_step, "serial_ms": t_serial, "overlapped_ms": t_over,
             "hidden_fraction_of_step": (t_serial - t_over) / t_step if t_step > 0 else None,
+            "block_budget_sweep": budgets,
             "synthetic_backward": f"bf16 GEMM {tokens} x {K} x n_b/1024 per bucket (~4*{tokens}*n_b FLOPs)",
-            "api": "zr_step_bucket per bucket on a side stream after the bucket's ready event"}
+            "api": "zr_step_bucket per bucket on a side stream after the bucket's ready event; the sweep caps each "
+                   "bucket launch with zr_plan_set_bucket_blocks"}
 
 
-def run_zr(args, w):
+def _link_rates(torch, host, dev_buf, dev, stream, max_bytes: int = 4 << 30, reps: int = 3):
+    """Host<->device copy bandwidth: `reps` copies of up to max_bytes between a pinned host tensor and a device
+    tensor, each direction timed with CUDA events on the launching stream."""
+    k = min(host.numel(), dev_buf.numel(), max_bytes // host.element_size())
+    h, d = host[:k], dev_buf[:k]
+    nbytes = k * host.element_size()
+    out = {}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        out[f"link_{name}_GBs"] = nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    out["link_copy_bytes"] = int(nbytes)
+    out["link_how"] = "pinned host <-> device tensor copy_ (one cudaMemcpyAsync), CUDA events, best-effort single stream"
+    return out
+
+
+def _setup(w, zr, zrgen, dev, stream, inplace_main):
+    """Plan, seeded state and step-1 gradients of workload w on the device."""
     import torch
-    ws, rank, local = _dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device(f"cuda:{local if ws > 1 else 0}")
-
-    import __graft_entry__
-    if rank == 0 or ws == 1:
-        __graft_entry__.build()
-    if ws > 1:
-        torch.distributed.barrier()
-        __graft_entry__.build()  # no-op once built
-    import zero_gradient_reduction_gb300 as zr
-    import zrgen
     from zrgen.layout import Layout
-
     plan = zr.Plan(list(w.tensors), W=w.W, A=w.A, dtype=w.dtype, stage=w.stage, cap=w.cap,
                    scaler=zr.Scaler(w.init_scale, w.dynamic))
     hyper = zr.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
     layout = Layout(w.tensors, plan.tensor_offsets, zrgen.sigma_per_tensor(w), w.seed, w.dtype, w.master_sigma)
-    stream = torch.cuda.current_stream(dev)
     cs = stream.cuda_stream
     table = torch.from_numpy(zrgen.normal_table().copy()).to(dev)
     n = plan.numel
     # the main step: ping-pong sets (zr_step), or one set stepped in place (zr_step_inplace) for a workload
     # whose two sets do not fit, or on request
-    inplace_main = args.inplace or w.state_sets == 1
     if inplace_main:
         state = plan.new_state1(dev)
         master0, param0 = state.master, state.param
@@ -342,6 +362,14 @@ def run_zr(args, w):
     for r in range(w.W * w.A):
         layout.grads_dev(grads[r], 1, r, w.init_scale, table, cs)
     torch.cuda.synchronize(dev)
+    return plan, hyper, state, grads
+
+
+def _measure_step(args, w, plan, hyper, state, grads, dev, stream, ws, gpu_index, inplace_main):
+    """The timed region: args.steps replays of the step captured as a CUDA graph, CUDA events on the launching
+    stream, clocks sampled throughout; re-taken once if a thermal or hardware slowdown was seen. Returns the
+    numbers of the JSON line for this workload."""
+    import torch
 
     def timed(k):
         if ws > 1:
@@ -370,7 +398,7 @@ def run_zr(args, w):
 
     attempts = 0
     while True:
-        sampler = ClockSampler(local if ws > 1 else 0)
+        sampler = ClockSampler(gpu_index)
         sampler.start()
         ms_total = timed(args.steps)
         clocks = sampler.stop()
@@ -380,6 +408,7 @@ def run_zr(args, w):
             break
     rep = plan.report(stream)
     assert rep.overflow == 0 and rep.steps == args.warmup + args.steps * attempts, rep.as_dict()
+    del graph
 
     ms_max = max_over_ranks(ms_total, ws, dev)
     ms_step = ms_max / args.steps
@@ -394,7 +423,83 @@ def run_zr(args, w):
         traffic, _digest = _traffic_record(w.name, "inplace_step", "traffic_bytes_per_step")
     else:
         traffic, _digest = _traffic_record(w.name)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "peak_source": f"{peak_kind} HBM copy bandwidth",
+                "frac_of_8tbs_nominal": achieved / 8000.0,
+                "kernel": "fused_step_kernel flag pass + in-place update (bytes and time of the step's two "
+                          "launches together)" if inplace_main else "fused_step_kernel (one launch per step)"}
+    clk = {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"), "reasons": clocks.get("reasons"),
+           "samples": clocks.get("samples"), "power_w_max": clocks.get("power_w_max"), "attempts": attempts}
+    return {"ms_step": ms_step, "value": value, "step_bytes": step_bytes, "achieved": achieved,
+            "roofline": roofline, "clocks": clk, "current": rep.current}
 
+
+def _measure_noalloc(zr, plan, hyper, state, grads, w, dev, stream, current, reps=10):
+    """zr_step_noalloc (scratch in a static device array, nothing allocated) against zr_step on the same
+    buffers, both launched eagerly, CUDA events on the launching stream. Every step here is clean, so the
+    caller-side live set flips after each call."""
+    import torch
+    of = torch.zeros(1, dtype=torch.int32, device=dev)
+    cur = current
+    for _ in range(3):
+        zr.step_noalloc(plan.buckets, w.W, w.A, w.dtype, grads, state, cur, hyper, w.init_scale, 1, of,
+                        stream=stream)
+        cur = 1 - cur
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(reps):
+        zr.step_noalloc(plan.buckets, w.W, w.A, w.dtype, grads, state, cur, hyper, w.init_scale, 2 + i, of,
+                        stream=stream)
+        cur = 1 - cur
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert int(of.item()) == 0
+    na_ms = e0.elapsed_time(e1) / reps
+    for _ in range(3):
+        plan.step(grads, state, hyper, stream=stream)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(reps):
+        plan.step(grads, state, hyper, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    st_ms = e0.elapsed_time(e1) / reps
+    return {"ms_per_step": na_ms, "zr_step_ms_per_step": st_ms, "ratio_to_zr_step": na_ms / st_ms,
+            "launches_per_step": 2, "steps": reps,
+            "call": "zr_step_noalloc (set-up launch + the fused kernel, eager) against zr_step (eager)"}
+
+
+def run_zr(args, w):
+    import torch
+    ws, rank, local = _dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device(f"cuda:{local if ws > 1 else 0}")
+    gpu_index = local if ws > 1 else 0
+
+    import __graft_entry__
+    if rank == 0 or ws == 1:
+        __graft_entry__.build()
+    if ws > 1:
+        torch.distributed.barrier()
+        __graft_entry__.build()  # no-op once built
+    import zero_gradient_reduction_gb300 as zr
+    import zrgen
+
+    stream = torch.cuda.current_stream(dev)
+    inplace_main = args.inplace or w.state_sets == 1
+    plan, hyper, state, grads = _setup(w, zr, zrgen, dev, stream, inplace_main)
+    n = plan.numel
+    main = _measure_step(args, w, plan, hyper, state, grads, dev, stream, ws, gpu_index, inplace_main)
+    ms_step, value, step_bytes = main["ms_step"], main["value"], main["step_bytes"]
+    peak, _ = _peaks()
+    rep = plan.report(stream)
     # the in-place step (zr_step_inplace: a flag pass, then AdamW in place on ONE state set, for runs with
     # no room for a second set), timed right after the step it is compared with, on the live set of the
     # ping-pong state so that it needs no memory of its own: (4*W*A + 26) bytes per param, two launches
@@ -562,9 +667,27 @@ def run_zr(args, w):
                               w.init_scale, 2 + i, nthreads, stream=stream)
         torch.cuda.synchronize(dev)
         o_ms = (time.perf_counter() - t0) / 2 * 1e3
+        # the host-side bounds of that step: the host AdamW alone (zr_offload_adamw: 4 + 12 bytes read, 12 + 2
+        # written per param of host memory) on the same arrays, and a plain multi-threaded host copy
+        t0 = time.perf_counter()
+        zr.offload_adamw(sums_host, h_master, h_m, h_v, param_host, w.dtype, hyper, w.init_scale, w.W, 4, nthreads)
+        ha_s = time.perf_counter() - t0
+        k = min(n, 1 << 30)
+        src = torch.from_numpy(h_m[:k])
+        dst = torch.from_numpy(h_v[:k])
+        dst.copy_(src)
+        t0 = time.perf_counter()
+        for _ in range(3):
+            dst.copy_(src)
+        hc_s = (time.perf_counter() - t0) / 3
         offload = {"ms_per_step": o_ms, "Gparams_per_s": plan.n_real / o_ms / 1e6, "host_threads": nthreads,
                    "link_bytes_per_param": 6, "host_state_GB": 12 * n / 1e9,
-                   "call": "zr_offload_step (reduce-scatter on GPU, AdamW on the host CPU, params back)"}
+                   "host_adamw_ms": ha_s * 1e3, "host_adamw_GBs": 30 * n / ha_s / 1e9,
+                   "host_copy_GBs": 8 * k / hc_s / 1e9, "host_copy_threads": torch.get_num_threads(),
+                   "call": "zr_offload_step (reduce-scatter on GPU, AdamW on the host CPU, params back); "
+                           "host_adamw: zr_offload_adamw alone on the same host arrays (30 B/param of host memory); "
+                           "host_copy: torch CPU copy_ of 4 GB fp32 (read + write bytes)"}
+        del src, dst
         del sums_dev, sums_host, param_host, h_master, h_m, h_v
 
     e2e = None
@@ -596,30 +719,59 @@ def run_zr(args, w):
         e2e = {"value": whole_job_rate(plan.n_real * args.e2e_steps, dt, ws), "unit": "Gparams/s",
                "h2d_bytes_per_step": int(2 * n * w.W * w.A), "d2h_bytes_per_step": int(__import__("ctypes").sizeof(r)),
                "ms_per_step": dt / args.e2e_steps * 1e3, "steps": args.e2e_steps, "api": api}
-        del host
+        # the host link itself: one large pinned copy per direction (cudaMemcpyAsync through torch), CUDA events
+        link = _link_rates(torch, host[0], grads[0], dev, stream)
+        e2e.update(link)
+        e2e["frac_of_link_h2d"] = (e2e["h2d_bytes_per_step"] / (e2e["ms_per_step"] * 1e-3) / 1e9) / link["link_h2d_GBs"]
+        del host, e2e_step
+        if not inplace_main:
+            del dgr
 
+    rep_buckets = plan.buckets
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         params, secs, what = oracle_sample(w, plan.buckets, plan.tensor_offsets, args.cpu_seconds)
         cpu = {"value": params / secs / 1e9, "unit": "Gparams/s", "cores": 1, "kind": "oracle",
                "sample": f"{what}, step 1 inputs; {secs:.1f} s single-threaded on the host"}
+
+    # the other workload held to the HBM target, timed the same way on its own buffers once this workload's
+    # are freed; with zr_step_noalloc beside it (its static scratch holds this workload's tile schedule)
+    second = None
+    if args.second and args.second != w.name and ws == 1:
+        del plan, state, grads
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        w2 = zrgen.workload(args.second)
+        plan2, hyper2, state2, grads2 = _setup(w2, zr, zrgen, dev, stream, False)
+        m2 = _measure_step(args, w2, plan2, hyper2, state2, grads2, dev, stream, ws, gpu_index, False)
+        noalloc = None
+        try:
+            noalloc = _measure_noalloc(zr, plan2, hyper2, state2, grads2, w2, dev, stream, m2["current"])
+        except Exception as ex:  # a workload beyond the static scratch is refused by the call itself
+            noalloc = {"unavailable": str(ex).splitlines()[0]}
+        second = {"config": _config(w2, plan2.buckets, f"inputs larger than L2: {m2['step_bytes'] / 1e9:.1f} GB "
+                                    "moved per step", launch="zr_step captured once as a CUDA graph, replayed once "
+                                    "per timed step"),
+                  "value": m2["value"], "unit": "Gparams/s", "ms_per_step": m2["ms_step"], "steps": args.steps,
+                  "warmup": args.warmup, "hbm_tbs": m2["achieved"] / 1e3, "roofline": m2["roofline"],
+                  "clocks": m2["clocks"], "gpu_launches": args.steps, "noalloc_step": noalloc}
+        plan2.close()
+        del plan2, state2, grads2
+    else:
+        plan.close()
 
     line = {
         "metric": "fused reduce-scatter+AdamW step Gparams/s", "value": value, "unit": "Gparams/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded Philox4x32-10 normal draws, the workload's shapes and sigmas)",
-        "config": _config(w, plan.buckets, f"inputs larger than L2: {step_bytes / 1e9:.1f} GB moved per step"
+        "config": _config(w, rep_buckets, f"inputs larger than L2: {step_bytes / 1e9:.1f} GB moved per step"
                           if step_bytes > 4 * 129e6 else
                           f"{step_bytes / 1e6:.0f} MB per step: L2-resident, reported, not an HBM figure",
                           launch="zr_step_inplace (flag pass + update) captured once as a CUDA graph, replayed once "
                           "per timed step" if inplace_main else
                           "zr_step captured once as a CUDA graph, replayed once per timed step", inplace=inplace_main),
-        "hbm_tbs": achieved / 1e3,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_source": f"{peak_kind} HBM copy bandwidth",
-                     "frac_of_8tbs_nominal": achieved / 8000.0,
-                     "kernel": "fused_step_kernel flag pass + in-place update (bytes and time of the step's two "
-                               "launches together)" if inplace_main else "fused_step_kernel (one launch per step)"},
+        "hbm_tbs": main["achieved"] / 1e3,
+        "roofline": main["roofline"],
         "cpu_baseline": cpu,
         "e2e": e2e,
         "unfused_chain": chain,
@@ -628,13 +780,13 @@ def run_zr(args, w):
         "bucketed_overlap": overlap,
         "zero_offload": offload,
         "gpu_launches": args.steps * (2 if inplace_main else 1),
-        "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
-                   "reasons": clocks.get("reasons"), "samples": clocks.get("samples"),
-                   "power_w_max": clocks.get("power_w_max"), "attempts": attempts},
+        "clocks": main["clocks"],
+        f"workload_{args.second}": second,
     }
+    if second is None:
+        del line[f"workload_{args.second}"]
     if rank == 0:
         print(json.dumps(line), flush=True)
-    plan.close()
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0
@@ -647,6 +799,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["zr", "reference"], default="zr")
     ap.add_argument("--workload", default=WORKLOAD_DEFAULT)
+    ap.add_argument("--second", default=None,
+                    help=f"a second workload timed after the first, on freed memory (default: {SECOND_DEFAULT} when "
+                         f"the workload is {WORKLOAD_DEFAULT}; 'none' for no second workload)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -661,6 +816,10 @@ def main():
         args.warmup = 3
     import zrgen
     w = zrgen.workload(args.workload)
+    if args.second is None:
+        args.second = SECOND_DEFAULT if args.workload == WORKLOAD_DEFAULT else None
+    elif args.second == "none":
+        args.second = None
     if args.impl == "reference":
         return run_reference(args, w)
     return run_zr(args, w)

@@ -275,6 +275,17 @@ zr_status zr_step_from_host(zr_plan* p, int stage, const void* const* host_grads
 zr_status zr_step_bucket(zr_plan* p, int stage, int bucket, const void* const* grads, const zr_state* st,
                          const zr_adamw_hyper* h, void* stream);
 
+/* How many thread blocks each zr_step_bucket launch of plan p may take, so that buckets
+ * stepped while backward is still running leave the other SMs to it (the pages' overlap
+ * moves gradients over links driven by a few SMs while the rest compute: [P1] 二, [P3]
+ * Overlap). max_blocks = 0, the default, gives each launch one block per tile (every
+ * block that fits at once for a small bucket); max_blocks > 0 caps each launch at that
+ * many blocks, which then stride over the bucket's tiles. The results are the same bytes
+ * for every value; only the launch shape changes. Call it between steps, never while a
+ * step's bucket launches are in flight (the step's last block is found by counting the
+ * blocks of all its launches). Errors: ZR_ERR_INVALID for a null plan or max_blocks < 0. */
+zr_status zr_plan_set_bucket_blocks(zr_plan* p, int max_blocks);
+
 /* The optimizer state and the parameter replica as ONE set (zr_step_inplace). Device
  * pointers, zr_plan_numel elements each; param is of the plan's dtype. */
 typedef struct {

@@ -14,6 +14,17 @@ import oracle
 from zrgen.layout import Layout, grad_stream, master_stream  # noqa: E402,F401
 
 
+def oracle_layout(plan, numels, cap: int, W: int):
+    """The oracle's own bucket table and tensor offsets for a layout (page "DP / DDP / DeepSpeed ZeRO-1/2/3",
+    section 二, and page "第 7 讲", DDP 核心实现细节: buckets in reverse registration order). Asserts that the
+    plan zr_plan_create built has the same, so that every oracle call and every oracle-side input uses a
+    table the product did not make."""
+    buckets, offsets = oracle.bucket_plan(list(numels), int(cap), int(W))
+    assert np.array_equal(np.asarray(plan.buckets), buckets), "zr_plan_create's buckets differ from the oracle's"
+    assert np.array_equal(np.asarray(plan.tensor_offsets), offsets), "zr_plan_create's offsets differ from the oracle's"
+    return buckets, offsets
+
+
 def sample_windows(buckets: np.ndarray, W: int, which, L: int = 256, rng=None, cover=()):
     """Index windows for the sampled buckets. Each window set is a mini-bucket: for every block c of
     the bucket, L consecutive flat indices inside block c (at its start, its end or a seeded point),

@@ -125,3 +125,18 @@ def test_argument_checks_without_gpu(zr):
     s1 = zr.StateC1(16, 16, 16, 16)
     assert L.zr_step_inplace(None, 2, ctypes.addressof(one), ctypes.byref(s1), ctypes.byref(h), None, None) == 1
     assert b"zr_step_inplace" in L.zr_last_error()
+
+
+def test_beta_and_cap_checks_without_gpu(zr):
+    """Betas outside [0, 1) are refused by every call that forms the bias corrections on the host (the
+    running product of the betas must settle for large t), and a negative block cap is refused."""
+    L = zr.lib()
+    for b1, b2 in ((1.0, 0.999), (0.9, -0.5), (float("nan"), 0.999), (0.9, 1.5)):
+        h = zr.Hyper(1e-3, b1, b2, 1e-8, 0.0)
+        assert L.zr_adamw_shard_step(16, 16, 16, 16, 8, ctypes.byref(h), 1.0, 1, 1, 16, None) == 1
+        assert b"betas" in L.zr_last_error()
+        of = ctypes.c_int32(0)
+        assert L.zr_offload_adamw(16, 16, 16, 16, None, 1, 8, ctypes.byref(h), 1.0, 1, 1, 1, ctypes.byref(of)) == 1
+        assert b"betas" in L.zr_last_error()
+    assert L.zr_plan_set_bucket_blocks(None, 0) == 1
+    assert b"null plan" in L.zr_last_error()

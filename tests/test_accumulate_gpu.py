@@ -9,6 +9,7 @@ import oracle
 import zero_gradient_reduction_gb300 as zr
 import zrgen
 from zrgen.layout import Layout
+from _harness import oracle_layout
 from test_parity_gpu import HYPER, OHYPER, assert_state_close, f32bits, to_dev16, u16
 
 pytestmark = pytest.mark.gpu
@@ -69,7 +70,8 @@ def test_accumulate_then_fp32_step_equals_fused_and_oracle(W, A):
     acc_plan = zr.Plan(numels, W=W, A=1, dtype=zr.BF16, stage=2, cap=50_000, order=order, scaler=zr.Scaler(1.0),
                        fp32_grads=True)
     assert np.array_equal(fused.buckets, acc_plan.buckets)
-    lay = Layout(numels, fused.tensor_offsets, sig, 5, zr.BF16)
+    obuckets, ooffsets = oracle_layout(fused, numels, 50_000, W)
+    lay = Layout(numels, ooffsets, sig, 5, zr.BF16)
     n = fused.numel
     table = torch.from_numpy(zrgen.normal_table().copy()).cuda()
     cs = torch.cuda.current_stream().cuda_stream
@@ -95,7 +97,7 @@ def test_accumulate_then_fp32_step_equals_fused_and_oracle(W, A):
             assert x.cpu().view(torch.int32 if x.element_size() == 4 else torch.int16).numpy().tobytes() == \
                 y.cpu().view(torch.int32 if y.element_size() == 4 else torch.int16).numpy().tobytes()
         og = [lay.grads_host(0, n, step, r, 1.0) for r in range(W * A)]
-        oracle.step(W, A, zr.BF16, fused.buckets, og, *o, OHYPER, osc, order=order)
+        oracle.step(W, A, zr.BF16, obuckets, og, *o, OHYPER, osc, order=order)
         L = st_a.live(ra.current)
         assert_state_close(L["master"].cpu().numpy(), L["m"].cpu().numpy(), L["v"].cpu().numpy(), u16(L["param"]),
                            *o, exact=True, where=f"W={W} A={A} step {step}: ")

@@ -6,6 +6,7 @@ import torch
 
 import oracle
 import zero_gradient_reduction_gb300 as zr
+from _harness import oracle_layout
 from test_parity_gpu import HYPER, OHYPER, assert_state_close, u16
 
 pytestmark = pytest.mark.gpu
@@ -130,7 +131,8 @@ def test_max_workers_and_replicas_with_empty_tensors():
         st.master[0].copy_(torch.from_numpy(master))
         rep = plan.step(grads, st, HYPER, report=True)
         o = [master.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16)]
-        orep, _ = oracle.step(W, A, zr.BF16, plan.buckets, hg, *o, OHYPER, oracle.new_scaler(1.0))
+        ob, _ = oracle_layout(plan, numels, 8_000, W)
+        orep, _ = oracle.step(W, A, zr.BF16, ob, hg, *o, OHYPER, oracle.new_scaler(1.0))
         assert rep.overflow == orep.overflow == 0
         L = st.live(rep.current)
         assert_state_close(L["master"].cpu().numpy(), L["m"].cpu().numpy(), L["v"].cpu().numpy(), u16(L["param"]),
@@ -149,7 +151,8 @@ def test_fp32_overflow_from_finite_bf16_skips():
     st.master[0].fill_(0.5)
     grads = [torch.from_numpy(g.view(np.int16).copy()).cuda().view(torch.bfloat16) for g in hg]
     rep = plan.step(grads, st, HYPER, report=True)
-    orep, _ = oracle.step(2, 1, zr.BF16, plan.buckets, hg, np.full(n, 0.5, np.float32), np.zeros(n, np.float32),
+    ob, _ = oracle_layout(plan, [n], n, 2)
+    orep, _ = oracle.step(2, 1, zr.BF16, ob, hg, np.full(n, 0.5, np.float32), np.zeros(n, np.float32),
                           np.zeros(n, np.float32), np.zeros(n, np.uint16), OHYPER, oracle.new_scaler(1.0, dynamic=True))
     assert rep.overflow == orep.overflow == 1 and rep.current == 0 and rep.t == 0
     plan.close()
@@ -167,7 +170,8 @@ def test_signed_zero_gradients():
     got = sums.cpu().numpy()
     assert np.all(got == 0) and np.all(np.signbit(got))
     z = np.zeros(n, np.float32)
-    _, want = oracle.step(3, 1, zr.F16, plan.buckets, hg, z.copy(), z.copy(), z.copy(), np.zeros(n, np.uint16),
+    ob, _ = oracle_layout(plan, [n], n, 3)
+    _, want = oracle.step(3, 1, zr.F16, ob, hg, z.copy(), z.copy(), z.copy(), np.zeros(n, np.uint16),
                           OHYPER, oracle.new_scaler(1.0), want_sums=True)
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
     plan.close()

@@ -47,8 +47,8 @@ class InPlaceRun(FusedRun):
 
 
 @pytest.mark.parametrize("W,A,dtype", [(1, 1, zr.BF16), (2, 1, zr.F16), (3, 1, zr.BF16), (5, 1, zr.F16),
-                                       (8, 1, zr.BF16), (2, 4, zr.BF16), (4, 4, zr.F16), (3, 3, zr.BF16),
-                                       (16, 1, zr.F16)])
+                                       (6, 1, zr.BF16), (7, 1, zr.F16), (8, 1, zr.BF16), (2, 4, zr.BF16),
+                                       (4, 4, zr.F16), (3, 3, zr.BF16), (16, 1, zr.F16), (17, 1, zr.BF16)])
 def test_inplace_ragged_buckets_bit_exact(W, A, dtype):
     rng = np.random.default_rng(W * 100 + A + 7)
     numels = [1000, 37, 5000, 8, 123_457, 64, 9_999, 3, 40_000]
@@ -68,7 +68,7 @@ def test_inplace_equals_pingpong_with_a_skip():
     kw = dict(cap=30_000, S=65536.0, dynamic=True, seed=6, interval=2)
     pp = FusedRun(numels, 4, 1, zr.F16, **kw)
     ip = InPlaceRun(numels, 4, 1, zr.F16, **kw)
-    inj = (2, int(pp.plan.tensor_offsets[2]) + 5)
+    inj = (2, int(pp.ooffsets[2]) + 5)
     for s in range(1, 6):
         rp, _ = pp.step(s, inject=inj if s == 2 else None)
         ri, _ = ip.step(s, inject=inj if s == 2 else None)
@@ -85,7 +85,7 @@ def test_inplace_skip_leaves_the_set_unchanged(dtype):
     run = InPlaceRun(numels, 2, 1, dtype, cap=25_000, S=65536.0, dynamic=True, seed=5)
     run.step(1)
     before = [x.copy() for x in run.live()]
-    rep, _ = run.step(2, inject=(1, int(run.plan.tensor_offsets[1]) + 99))
+    rep, _ = run.step(2, inject=(1, int(run.ooffsets[1]) + 99))
     assert rep.overflow == 1 and rep.skipped == 1 and rep.t == 1 and rep.scale == 32768.0
     for a, b in zip(run.live(), before):
         assert a.tobytes() == b.tobytes()
@@ -185,7 +185,9 @@ def test_inplace_max_workers_and_replicas_with_empty_tensors():
         one.master.copy_(torch.from_numpy(master))
         rep = plan.step_inplace(grads, one, HYPER, report=True)
         o = [master.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16)]
-        orep, _ = oracle.step(W, A, zr.BF16, plan.buckets, hg, *o, OHYPER, oracle.new_scaler(1.0))
+        from _harness import oracle_layout
+        ob, _ = oracle_layout(plan, numels, 8_000, W)
+        orep, _ = oracle.step(W, A, zr.BF16, ob, hg, *o, OHYPER, oracle.new_scaler(1.0))
         assert rep.overflow == orep.overflow == 0 and rep.t == 1
         assert_state_close(one.master.cpu().numpy(), one.m.cpu().numpy(), one.v.cpu().numpy(),
                            one.param.cpu().view(torch.int16).numpy().view(np.uint16), *o, exact=True,
@@ -247,7 +249,7 @@ def test_inplace_checkpoint_resume_is_byte_identical():
     numels = [30_000, 5_000, 17_000]
     kw = dict(cap=25_000, S=65536.0, dynamic=True, seed=9, interval=2)
     straight = InPlaceRun(numels, 2, 1, zr.F16, **kw)
-    inj = (0, int(straight.plan.tensor_offsets[1]) + 7)
+    inj = (0, int(straight.ooffsets[1]) + 7)
     for s in range(1, 5):
         straight.step(s, inject=inj if s == 2 else None)
     first = InPlaceRun(numels, 2, 1, zr.F16, **kw)

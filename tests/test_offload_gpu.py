@@ -8,6 +8,7 @@ import oracle
 import zero_gradient_reduction_gb300 as zr
 import zrgen
 from zrgen.layout import Layout
+from _harness import oracle_layout
 from test_parity_gpu import OHYPER, u16
 
 pytestmark = pytest.mark.gpu
@@ -29,7 +30,8 @@ def test_offload_step_matches_oracle(W, dtype):
     S = 1024.0 if dtype == zr.F16 else 1.0
     plan = zr.Plan(numels, W=W, dtype=dtype, stage=2, cap=200_000, order=list(range(W))[::-1])
     n = plan.numel
-    lay = Layout(numels, plan.tensor_offsets, np.full(len(numels), 1e-2, F32), 6, dtype)
+    ob, ooff = oracle_layout(plan, numels, 200_000, W)
+    lay = Layout(numels, ooff, np.full(len(numels), 1e-2, F32), 6, dtype)
     table = torch.from_numpy(zrgen.normal_table().copy()).cuda()
     cs = torch.cuda.current_stream().cuda_stream
     tdt = plan.torch_dtype()
@@ -54,7 +56,7 @@ def test_offload_step_matches_oracle(W, dtype):
         of = plan.offload_step(grads, sums_dev, sums_host, master, m, v, param_host, param_dev, zr.AdamW(), S,
                                t + 1, nthreads=8)
         torch.cuda.synchronize()
-        rep, _ = oracle.step(W, 1, dtype, plan.buckets, og, *o, OHYPER, osc, order=list(range(W))[::-1])
+        rep, _ = oracle.step(W, 1, dtype, ob, og, *o, OHYPER, osc, order=list(range(W))[::-1])
         assert of == rep.overflow == (1 if step == 2 else 0)
         if of:
             assert master.tobytes() == before
@@ -83,7 +85,8 @@ def test_offload_random_plans_and_thread_counts(case):
     plan = zr.Plan(numels, W=W, dtype=dtype, stage=2, cap=cap, order=order)
     n = plan.numel
     tdt = plan.torch_dtype()
-    lay = Layout(numels, plan.tensor_offsets, np.full(len(numels), 1e-2, F32), 40 + case, dtype)
+    ob, ooff = oracle_layout(plan, numels, cap, W)
+    lay = Layout(numels, ooff, np.full(len(numels), 1e-2, F32), 40 + case, dtype)
     table = torch.from_numpy(zrgen.normal_table().copy()).cuda()
     cs = torch.cuda.current_stream().cuda_stream
     grads = [torch.zeros(n, dtype=tdt, device="cuda") for _ in range(W)]
@@ -100,7 +103,7 @@ def test_offload_random_plans_and_thread_counts(case):
     of = plan.offload_step(grads, sums_dev, sums_host, master, m, v, param_host, param_dev, zr.AdamW(), 1.0, 1,
                            nthreads=nthreads)
     torch.cuda.synchronize()
-    rep, _ = oracle.step(W, 1, dtype, plan.buckets, og, *o, OHYPER, oracle.new_scaler(1.0), order=order)
+    rep, _ = oracle.step(W, 1, dtype, ob, og, *o, OHYPER, oracle.new_scaler(1.0), order=order)
     assert of == rep.overflow == 0
     for a, b in zip((master, m, v), o[:3]):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (case, W, cap, nthreads)

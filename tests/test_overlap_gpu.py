@@ -9,6 +9,7 @@ import oracle
 import zero_gradient_reduction_gb300 as zr
 import zrgen
 from zrgen.layout import Layout
+from _harness import oracle_layout
 from test_parity_gpu import HYPER, OHYPER, assert_state_close, u16
 
 pytestmark = pytest.mark.gpu
@@ -27,7 +28,8 @@ def _gpu():
 
 def _setup(W=3, dtype=zr.F16, S=1024.0, dynamic=False):
     plans = [zr.Plan(NUMELS, W=W, dtype=dtype, stage=2, cap=35_000, scaler=zr.Scaler(S, dynamic)) for _ in range(2)]
-    lay = Layout(NUMELS, plans[0].tensor_offsets, np.full(len(NUMELS), 1e-2, F32), 3, dtype)
+    _, ooff = oracle_layout(plans[0], NUMELS, 35_000, W)
+    lay = Layout(NUMELS, ooff, np.full(len(NUMELS), 1e-2, F32), 3, dtype)
     table = torch.from_numpy(zrgen.normal_table().copy()).cuda()
     states = []
     for p in plans:
@@ -57,6 +59,34 @@ def test_bucketed_equals_single_launch():
         rb = plans[1].report()
         assert (ra.current, ra.t, ra.overflow, ra.steps) == (rb.current, rb.t, rb.overflow, rb.steps)
         assert _live_bytes(sa, ra.current) == _live_bytes(sb, rb.current)
+
+
+@pytest.mark.parametrize("cap", [1, 3, 16])
+def test_bucket_block_cap_gives_the_same_bytes(cap):
+    """zr_plan_set_bucket_blocks only changes the launch shape: every bucket launch capped at `cap` blocks
+    (striding over its tiles) computes what one zr_step computes."""
+    plans, lay, table, (sa, sb) = _setup()
+    plans[1].set_bucket_blocks(cap)
+    n = plans[0].numel
+    grads = [torch.zeros(n, dtype=torch.float16, device="cuda") for _ in range(3)]
+    cs = torch.cuda.current_stream().cuda_stream
+    for step in (1, 2):
+        for r in range(3):
+            lay.grads_dev(grads[r], step, r, 1024.0, table, cs)
+        ra = plans[0].step(grads, sa, HYPER, report=True)
+        for b in range(len(plans[1].buckets)):
+            plans[1].step_bucket(b, grads, sb, HYPER)
+        rb = plans[1].report()
+        assert (ra.current, ra.t, ra.overflow, ra.steps) == (rb.current, rb.t, rb.overflow, rb.steps)
+        assert _live_bytes(sa, ra.current) == _live_bytes(sb, rb.current)
+    plans[1].set_bucket_blocks(0)  # back to one block per tile, between steps
+    ra = plans[0].step(grads, sa, HYPER, report=True)
+    for b in range(len(plans[1].buckets)):
+        plans[1].step_bucket(b, grads, sb, HYPER)
+    rb = plans[1].report()
+    assert ra.steps == rb.steps == 3 and _live_bytes(sa, ra.current) == _live_bytes(sb, rb.current)
+    with pytest.raises(zr.ZrError):
+        plans[1].set_bucket_blocks(-1)
 
 
 def test_bucketed_skip_is_global():
@@ -95,13 +125,14 @@ def test_overlapped_schedule_matches_oracle():
     om = lay.master_host(0, n)
     o = [om, np.zeros(n, F32), np.zeros(n, F32), np.zeros(n, np.uint16)]
     osc = oracle.new_scaler(1.0)
-    by_off = sorted(range(len(NUMELS)), key=lambda t: p.tensor_offsets[t])
+    ob, ooff = oracle_layout(p, NUMELS, 35_000, W)
+    by_off = sorted(range(len(NUMELS)), key=lambda t: ooff[t])
     for step in (1, 2):
         events = []
-        for b, (s0, ln, _) in enumerate(p.buckets):
+        for b, (s0, ln, _) in enumerate(ob):
             with torch.cuda.stream(compute):
                 for t in by_off:  # "backward" writes this bucket's tensors
-                    off = int(p.tensor_offsets[t])
+                    off = int(ooff[t])
                     if s0 <= off < s0 + ln:
                         for r in range(W):
                             zrgen.fill_dev(grads[r].data_ptr() + 2 * off, NUMELS[t], zrgen.BF16, 3,
@@ -114,7 +145,7 @@ def test_overlapped_schedule_matches_oracle():
         torch.cuda.synchronize()
         rep = p.report()
         og = [lay.grads_host(0, n, step, r, 1.0) for r in range(W)]
-        oracle.step(W, 1, zr.BF16, p.buckets, og, *o, OHYPER, osc)
+        oracle.step(W, 1, zr.BF16, ob, og, *o, OHYPER, osc)
         L = sa.live(rep.current)
         assert_state_close(L["master"].cpu().numpy(), L["m"].cpu().numpy(), L["v"].cpu().numpy(),
                            u16(L["param"]), *o, exact=True, where=f"overlapped step {step}: ")

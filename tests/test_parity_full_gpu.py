@@ -14,7 +14,7 @@ import torch
 import oracle
 import zero_gradient_reduction_gb300 as zr
 import zrgen
-from _harness import Layout, OracleWindows, sample_windows
+from _harness import Layout, OracleWindows, oracle_layout, sample_windows
 from test_parity_gpu import HYPER, OHYPER, assert_state_close, u16
 
 pytestmark = pytest.mark.gpu
@@ -37,7 +37,8 @@ def run_sampled(w: zrgen.Workload, steps=None, extra_buckets=3, inplace=False):
     steps = steps or w.steps
     plan = zr.Plan(list(w.tensors), W=w.W, A=w.A, dtype=w.dtype, stage=w.stage, cap=w.cap,
                    scaler=zr.Scaler(w.init_scale, w.dynamic))
-    layout = Layout(w.tensors, plan.tensor_offsets, zrgen.sigma_per_tensor(w), w.seed, w.dtype, w.master_sigma)
+    obuckets, ooffsets = oracle_layout(plan, w.tensors, w.cap, w.W)
+    layout = Layout(w.tensors, ooffsets, zrgen.sigma_per_tensor(w), w.seed, w.dtype, w.master_sigma)
     cs = torch.cuda.current_stream().cuda_stream
     table = torch.from_numpy(zrgen.normal_table().copy()).cuda()
     n = plan.numel
@@ -48,7 +49,7 @@ def run_sampled(w: zrgen.Workload, steps=None, extra_buckets=3, inplace=False):
     zr.all_gather(master0, [state.param if inplace else state.param[0]])
     grads = [torch.zeros(n, dtype=plan.torch_dtype(), device="cuda") for _ in range(w.W * w.A)]
 
-    nb = len(plan.buckets)
+    nb = len(obuckets)
     rng = np.random.default_rng(w.seed + 17)
     if nb <= 8:
         which = list(range(nb))
@@ -59,8 +60,8 @@ def run_sampled(w: zrgen.Workload, steps=None, extra_buckets=3, inplace=False):
         site = zrgen.inject_site(w, s)
         if site is not None:
             wk, t, i = site
-            inject_flat[s] = (wk * w.A, int(plan.tensor_offsets[t]) + i)
-    windows = sample_windows(plan.buckets, w.W, which, cover=[v[1] for v in inject_flat.values()])
+            inject_flat[s] = (wk * w.A, int(ooffsets[t]) + i)
+    windows = sample_windows(obuckets, w.W, which, cover=[v[1] for v in inject_flat.values()])
     ow = OracleWindows(layout, windows, w.W, w.A, OHYPER, oracle.new_scaler(w.init_scale, w.dynamic))
     idx_all = torch.from_numpy(np.concatenate([ix for ix, _ in windows])).cuda()
     bounds = np.cumsum([0] + [len(ix) for ix, _ in windows])

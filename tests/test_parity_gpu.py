@@ -13,7 +13,7 @@ import torch
 import oracle
 import zero_gradient_reduction_gb300 as zr
 import zrgen
-from _harness import Layout
+from _harness import Layout, oracle_layout
 
 pytestmark = pytest.mark.gpu
 
@@ -256,8 +256,9 @@ class FusedRun:
         self.plan = zr.Plan(numels, W=W, A=A, dtype=dtype, stage=stage, cap=cap, order=order,
                             scaler=zr.Scaler(S, dynamic, growth_interval=interval))
         self.W, self.A, self.dtype, self.order = W, A, dtype, order
+        self.obuckets, self.ooffsets = oracle_layout(self.plan, numels, cap, W)
         sig = np.full(len(numels), 1e-2, F32) if sigma is None else np.asarray(sigma, F32)
-        self.layout = Layout(numels, self.plan.tensor_offsets, sig, seed, dtype)
+        self.layout = Layout(numels, self.ooffsets, sig, seed, dtype)
         n = self.plan.numel
         self.n = n
         self.table = torch.from_numpy(zrgen.normal_table().copy()).cuda()
@@ -285,7 +286,7 @@ class FusedRun:
             self.grads[r].view(torch.int16)[i] = np.int16(np.uint16(bits).view(np.int16))
             ograds[r][i] = bits
         rep = self._launch(stage)
-        orep, _ = oracle.step(self.W, self.A, self.dtype, self.plan.buckets, ograds, *self.o, OHYPER, self.osc,
+        orep, _ = oracle.step(self.W, self.A, self.dtype, self.obuckets, ograds, *self.o, OHYPER, self.osc,
                               order=self.order)
         assert rep.overflow == orep.overflow and rep.skipped == orep.skipped
         assert rep.scale_used == orep.scale_used and rep.scale == orep.scale_next
@@ -317,9 +318,10 @@ def test_fused_tiny_config_bit_exact():
         run.check(f"step {s}: ")
 
 
-@pytest.mark.parametrize("W,A,dtype", [(2, 1, zr.F16), (3, 1, zr.BF16), (5, 1, zr.F16), (8, 1, zr.BF16),
-                                       (2, 4, zr.BF16), (4, 4, zr.F16), (8, 4, zr.BF16), (3, 3, zr.BF16),
-                                       (16, 1, zr.F16)])
+@pytest.mark.parametrize("W,A,dtype", [(2, 1, zr.F16), (3, 1, zr.BF16), (5, 1, zr.F16), (6, 1, zr.BF16),
+                                       (7, 1, zr.F16), (8, 1, zr.BF16), (2, 4, zr.BF16), (4, 4, zr.F16),
+                                       (8, 4, zr.BF16), (3, 3, zr.BF16), (9, 1, zr.BF16), (16, 1, zr.F16),
+                                       (17, 1, zr.BF16), (24, 1, zr.F16), (33, 1, zr.BF16)])
 def test_fused_ragged_buckets(W, A, dtype):
     rng = np.random.default_rng(W * 100 + A)
     numels = [1000, 37, 5000, 8, 123_457, 64, 9_999, 3, 40_000]
@@ -338,7 +340,7 @@ def test_fused_skip_then_resume():
     run.step(1)
     before = [x.copy() for x in run.live()]
     cur = run.current
-    rep, orep = run.step(2, inject=(1, int(run.plan.tensor_offsets[2]) + 123))
+    rep, orep = run.step(2, inject=(1, int(run.ooffsets[2]) + 123))
     assert rep.overflow == 1 and rep.skipped == 1 and rep.current == cur and rep.t == 1
     assert rep.scale == 32768.0 and rep.skipped_total == 1
     after = run.live()
@@ -447,7 +449,7 @@ def test_checkpoint_resume_is_byte_identical():
     plan and state, run steps 3-4: the live state matches byte for byte, with a skip in between."""
     numels = [30_000, 5_000, 17_000]
     straight = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=9, interval=2)
-    inj = (0, int(straight.plan.tensor_offsets[1]) + 7)
+    inj = (0, int(straight.ooffsets[1]) + 7)
     for s in range(1, 5):
         straight.step(s, inject=inj if s == 2 else None)
     first = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=9, interval=2)

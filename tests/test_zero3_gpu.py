@@ -6,6 +6,7 @@ import torch
 
 import oracle
 import zero_gradient_reduction_gb300 as zr
+from _harness import oracle_layout
 import zrgen
 from test_parity_gpu import HYPER, u16
 
@@ -32,12 +33,13 @@ def _bits(x: np.ndarray, dtype: int) -> torch.Tensor:
 def test_shard_and_gather_match_oracle(W, order_seed):
     rng = np.random.default_rng(order_seed)
     numels = [int(x) for x in rng.integers(1, 40_000, size=9)]
-    order = list(rng.permutation(W))
+    order = [int(x) for x in rng.permutation(W)]
     plan = zr.Plan(numels, W=W, A=1, dtype=zr.BF16, stage=3, cap=30_000, order=order)
     n = plan.numel
-    assert [plan.shard_numel(w) for w in range(W)] == oracle.shard_sizes(plan.buckets, W, order)
+    ob, _ = oracle_layout(plan, numels, 30_000, W)
+    assert [plan.shard_numel(w) for w in range(W)] == oracle.shard_sizes(ob, W, order)
     replica = rng.integers(0, 65536, size=n).astype(np.uint16)
-    want = oracle.shard_params(W, plan.buckets, replica, order)
+    want = oracle.shard_params(W, ob, replica, order)
     shards = plan.new_shards()
     plan.shard_params(_bits(replica, zr.BF16), shards)
     torch.cuda.synchronize()
@@ -53,7 +55,7 @@ def test_shard_and_gather_match_oracle(W, order_seed):
         out = torch.full((n,), 0, dtype=torch.int16, device="cuda")
         out.fill_(7)
         ref = np.full(n, 7, np.uint16)
-        oracle.param_all_gather(W, plan.buckets, want, ref, lo, hi, order)
+        oracle.param_all_gather(W, ob, want, ref, lo, hi, order)
         plan.gather_params(shards, out.view(torch.bfloat16), lo, hi)
         torch.cuda.synchronize()
         assert np.array_equal(u16(out), ref), (lo, hi)
@@ -93,8 +95,9 @@ def test_1p3b_layout_gather_sampled():
     torch.cuda.synchronize()
     assert torch.equal(out, full)
     # spot-check the layout against the oracle's definition on bucket 3's blocks
+    ob, _ = oracle_layout(plan, w.tensors, w.cap, w.W)
     b = 3
-    s0, ln, C = (int(x) for x in plan.buckets[b])
+    s0, ln, C = (int(x) for x in ob[b])
     for pos in range(w.W):
         blk = (pos + 1) % w.W
         lo, hi = min(blk * C, ln), min((blk + 1) * C, ln)

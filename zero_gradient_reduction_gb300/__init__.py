@@ -98,6 +98,7 @@ def lib():
                 "zr_all_reduce": (st, [vp, i32, i64, i32, vp, vp, i32, vp, vp]),
                 "zr_accumulate": (st, [vp, i32, vp, i64, i32, vp]),
                 "zr_step_bucket": (st, [vp, i32, i32, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp]),
+                "zr_plan_set_bucket_blocks": (st, [vp, i32]),
                 "zr_offload_adamw": (st, [vp, vp, vp, vp, vp, i32, i64, ctypes.POINTER(Hyper), ctypes.c_float, i32,
                                           i64, i32, ctypes.POINTER(ctypes.c_int32)]),
                 "zr_offload_step": (st, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(Hyper),
@@ -445,6 +446,10 @@ class Plan:
         h = hyper.c()
         _check(lib().zr_step_bucket(self._h, int(stage if stage is not None else self.stage), int(bucket),
                                     ctypes.addressof(arr), ctypes.byref(st), ctypes.byref(h), _stream_handle(stream)))
+
+    def set_bucket_blocks(self, max_blocks: int) -> None:
+        """Cap every zr_step_bucket launch at max_blocks thread blocks (0: no cap), between steps."""
+        _check(lib().zr_plan_set_bucket_blocks(self._h, int(max_blocks)))
 
     def step_overlapped(self, grads: Sequence, state: State, hyper: AdamW, ready_events: Sequence, side_stream,
                         stage: Optional[int] = None) -> None:

@@ -33,6 +33,16 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) % 16 == 0, "Ctrl is read and written as 16-byte words");
 
+// beta^n as the running product the fused step keeps in its control block (one double
+// multiplication per clean step, from 1.0), continued from p = beta^k (k <= n). The walk
+// stops once the product no longer changes: for 0 <= beta < 1 it settles at zero or at a
+// subnormal fixed point (after about 745 / (1 - beta) factors), so any n costs at most that.
+double beta_power_from(double p, int64_t k, float beta, int64_t n);
+// fp32(1 - beta^t), the bias correction of update t.
+float bias_correction_host(float beta, int64_t t);
+// 0 <= beta < 1 for both betas (what the host-side powers above need to terminate early).
+bool betas_ok(const zr_adamw_hyper& h);
+
 // The host AdamW of ZeRO-Offload (zr_offload_host.cpp): its constants for one step, and
 // the update plus 16-bit cast of elements [lo, hi), for callers that run their own threads.
 struct OffloadConsts {

@@ -120,6 +120,38 @@ __global__ void setup_tiles_kernel(const __grid_constant__ SetupArgs a) {
   }
 }
 
+// beta1^(t-1) and beta2^(t-1) as the running products a plan keeps, so that the bias
+// corrections match zr_step's bit for bit. The last result is kept per process: a caller
+// stepping t = 1, 2, 3, ... extends it by one factor per call instead of redoing t - 1
+// multiplications; going back in t, or other betas, starts again from 1.0 (bounded by
+// the fixed point of zr::beta_power_from).
+struct PowCache {
+  float beta1 = 0.0f, beta2 = 0.0f;
+  int64_t n = -1;  // exponent of the cached products (-1: empty)
+  double p1 = 1.0, p2 = 1.0;
+};
+std::mutex g_pow_mu;
+PowCache g_pow;
+
+void beta_powers(float beta1, float beta2, int64_t n, double* p1, double* p2) {
+  std::lock_guard<std::mutex> lock(g_pow_mu);
+  PowCache& c = g_pow;
+  const bool same = c.n >= 0 && std::memcmp(&c.beta1, &beta1, sizeof(float)) == 0 &&
+                    std::memcmp(&c.beta2, &beta2, sizeof(float)) == 0;
+  if (!same || c.n > n) {
+    c.beta1 = beta1;
+    c.beta2 = beta2;
+    c.n = 0;
+    c.p1 = 1.0;
+    c.p2 = 1.0;
+  }
+  c.p1 = zr::beta_power_from(c.p1, c.n, beta1, n);
+  c.p2 = zr::beta_power_from(c.p2, c.n, beta2, n);
+  c.n = n;
+  *p1 = c.p1;
+  *p2 = c.p2;
+}
+
 // Tiles the ring blocks of the buckets need at `tile` elements per tile.
 int64_t count_tiles(const zr_bucket* buckets, int nbuckets, int W, int64_t tile) {
   int64_t n = 0;
@@ -149,6 +181,7 @@ extern "C" zr_status zr_step_noalloc(const zr_bucket* buckets, int nbuckets, int
   if (!grads || !st || !h || !overflow) return fail(ZR_ERR_INVALID, "zr_step_noalloc: null argument");
   if (current != 0 && current != 1) return fail(ZR_ERR_INVALID, "zr_step_noalloc: current must be 0 or 1");
   if (t < 1) return fail(ZR_ERR_INVALID, "zr_step_noalloc: t must be >= 1");
+  if (!zr::betas_ok(*h)) return fail(ZR_ERR_INVALID, "zr_step_noalloc: betas must lie in [0, 1)");
   if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale))
     return fail(ZR_ERR_INVALID, "zr_step_noalloc: loss_scale must be positive and finite");
   if (reinterpret_cast<uintptr_t>(overflow) & 3u) return fail(ZR_ERR_INVALID, "zr_step_noalloc: misaligned overflow");
@@ -195,19 +228,20 @@ extern "C" zr_status zr_step_noalloc(const zr_bucket* buckets, int nbuckets, int
   if (ntiles > ZR_NOALLOC_MAX_TILES)
     return fail(ZR_ERR_INVALID, "zr_step_noalloc: the buckets need more than %d tiles of %lld elements "
                 "(the static scratch limit); use zr_plan_create/zr_step", ZR_NOALLOC_MAX_TILES, (long long)tile);
-  if (ntiles == 0) return ZR_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (ntiles == 0) {
+    // nothing to reduce: the step is clean, and the flag says so
+    e = cudaMemsetAsync(overflow, 0, sizeof(int32_t), cs);
+    return e == cudaSuccess ? ZR_OK : fail(ZR_ERR_CUDA, "zr_step_noalloc: %s", cudaGetErrorString(e));
+  }
 
   void* scratch = nullptr;
   zr_status s = scratch_address(&scratch);
   if (s != ZR_OK) return s;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
   // the tile schedule and the control block: one set-up launch per group of kSetupBuckets buckets
   double prod1 = 1.0, prod2 = 1.0;  // beta^(t-1): the step kernel takes the t-th factor itself
-  for (int64_t i = 1; i < t; ++i) {
-    prod1 = prod1 * (double)h->beta1;
-    prod2 = prod2 * (double)h->beta2;
-  }
+  beta_powers(h->beta1, h->beta2, t - 1, &prod1, &prod2);
   int32_t first = 0;
   for (int b0 = 0; b0 < nbuckets; b0 += kSetupBuckets) {
     SetupArgs sa;

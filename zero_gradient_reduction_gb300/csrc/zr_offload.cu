@@ -39,6 +39,7 @@ extern "C" zr_status zr_offload_step(zr_plan* p, int stage, const void* const* g
   if (stage < 0 || stage > 3) return fail(ZR_ERR_INVALID, "zr_offload_step: stage=%d not in 0..3", stage);
   if (p->A != 1) return fail(ZR_ERR_UNSUPPORTED, "zr_offload_step: plans with A > 1 (accumulate first)");
   if (t < 1) return fail(ZR_ERR_INVALID, "zr_offload_step: t must be >= 1");
+  if (!zr::betas_ok(*h)) return fail(ZR_ERR_INVALID, "zr_offload_step: betas must lie in [0, 1)");
   if (!zr::aligned16(sums_dev) || !zr::aligned16(param_dev))
     return fail(ZR_ERR_INVALID, "zr_offload_step: misaligned device buffer");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

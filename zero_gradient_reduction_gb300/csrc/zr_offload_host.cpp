@@ -108,7 +108,6 @@ void parallel_for(int64_t n, int nthreads, F fn) {
 }  // namespace
 
 namespace zr {
-float bias_correction_host(float beta, int64_t t);
 
 OffloadConsts offload_consts(const zr_adamw_hyper& h, float loss_scale, int W, int64_t t) {
   OffloadConsts k;
@@ -137,6 +136,7 @@ extern "C" zr_status zr_offload_adamw(const float* sums, float* master, float* m
                                       int64_t t, int nthreads, int32_t* overflow) {
   zr::clear_error();
   if (n < 0 || W < 1 || t < 1 || !h || !overflow) return fail(ZR_ERR_INVALID, "zr_offload_adamw: bad n/W/t or null");
+  if (!zr::betas_ok(*h)) return fail(ZR_ERR_INVALID, "zr_offload_adamw: betas must lie in [0, 1)");
   if (dt != ZR_F16 && dt != ZR_BF16) return fail(ZR_ERR_INVALID, "zr_offload_adamw: dtype must be F16 or BF16");
   if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale))
     return fail(ZR_ERR_INVALID, "zr_offload_adamw: loss_scale must be positive and finite");

@@ -24,7 +24,6 @@
 using zr::fail;
 
 namespace zr {
-float bias_correction_host(float beta, int64_t t);
 }
 
 #include "zr_plan.h"
@@ -53,6 +52,20 @@ zr_status cuda_fail(const char* what, cudaError_t e) {
 }
 
 }  // namespace
+
+// Blocks of each zr_step_bucket launch: one per tile (or a persistent grid for a small
+// bucket), capped at max_blocks if that is > 0; a step's launches add up to bucket_blocks.
+static void set_bucket_grids(zr_plan* p, int max_blocks) {
+  p->bucket_grid.clear();
+  p->bucket_blocks = 0;
+  for (size_t b = 0; b + 1 < p->tile_begin.size(); ++b) {
+    const int64_t nt = p->tile_begin[b + 1] - p->tile_begin[b];
+    int g = nt > 0 ? zr::step_grid(p, nt) : 0;  // a bucket without tiles launches nothing
+    if (max_blocks > 0 && g > max_blocks) g = max_blocks;
+    p->bucket_grid.push_back(g);
+    p->bucket_blocks += (unsigned)g;
+  }
+}
 
 extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   zr::clear_error();
@@ -163,11 +176,7 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   p->tile_begin.push_back(p->ntiles);
   p->resident = full;
   p->grid = zr::step_grid(p, p->ntiles);
-  for (size_t b = 0; b + 1 < p->tile_begin.size(); ++b) {
-    const int64_t nt = p->tile_begin[b + 1] - p->tile_begin[b];
-    p->bucket_grid.push_back(nt > 0 ? zr::step_grid(p, nt) : 0);  // a bucket without tiles launches nothing
-    p->bucket_blocks += (unsigned)p->bucket_grid.back();
-  }
+  set_bucket_grids(p, 0);
   if (e == cudaSuccess && !tiles.empty()) e = cudaMalloc(&p->tiles_dev, tiles.size() * sizeof(int4));
   if (e == cudaSuccess && !tiles.empty())
     e = cudaMemcpy(p->tiles_dev, tiles.data(), tiles.size() * sizeof(int4), cudaMemcpyHostToDevice);
@@ -340,6 +349,14 @@ extern "C" zr_status zr_step_bucket(zr_plan* p, int stage, int bucket, const voi
     return fail(ZR_ERR_INVALID, "zr_step_bucket: bucket %d outside [0, %d)", bucket, (int)p->buckets.size());
   return launch_step(p, stage, grads, st, h, static_cast<cudaStream_t>(stream), p->tile_begin[bucket],
                      p->tile_begin[bucket + 1], p->bucket_grid[bucket], p->bucket_blocks);
+}
+
+extern "C" zr_status zr_plan_set_bucket_blocks(zr_plan* p, int max_blocks) {
+  zr::clear_error();
+  if (!p) return fail(ZR_ERR_INVALID, "zr_plan_set_bucket_blocks: null plan");
+  if (max_blocks < 0) return fail(ZR_ERR_INVALID, "zr_plan_set_bucket_blocks: max_blocks=%d < 0", max_blocks);
+  set_bucket_grids(p, max_blocks);
+  return ZR_OK;
 }
 
 extern "C" zr_status zr_step_from_host(zr_plan* p, int stage, const void* const* host_grads, void* const* dev_grads,

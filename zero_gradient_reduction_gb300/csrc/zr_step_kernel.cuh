@@ -178,19 +178,25 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
     const int4 d = a.tiles[tile];
     const int64_t start = (int64_t)(((uint64_t)(uint32_t)d.y << 32) | (uint32_t)d.x);
     const int groups = d.z, c = d.w;
-    if (WT > 0 && AT == 1 && GT == DT) {
-      constexpr int WN = WT > 0 ? WT : 1;
+    if (WT != 0 && AT == 1 && GT == DT) {
+      // WT > 0: W known at compile time; WT < 0: any W <= 8, the missing replicas' loads
+      // and additions predicated off (W is uniform, so no lane diverges).
+      constexpr int WN = WT > 0 ? WT : 8;
       const uint16_t* gp[WN];
 #pragma unroll
       for (int h = 0; h < WN; ++h) {
-        int pos = c + h;
-        pos -= pos >= WN ? WN : 0;
-        gp[h] = static_cast<const uint16_t*>(a.grads[a.order[pos]]) + start;
+        if (WT > 0 || h < W) {
+          int pos = c + h;  // c < W and h < W
+          pos -= pos >= W ? W : 0;
+          gp[h] = static_cast<const uint16_t*>(a.grads[a.order[pos]]) + start;
+        } else {
+          gp[h] = nullptr;
+        }
       }
       // U groups per thread and iteration, all of their loads issued before any arithmetic:
       // with few replicas one group holds too few bytes in flight to cover HBM latency. The
       // flag pass has no state loads and registers to spare: 8/W groups (128 bytes in flight).
-      constexpr int UN = MODE == kFlagPass ? (WN >= 8 ? 1 : 8 / WN) : (WN <= 3 ? 2 : 1);
+      constexpr int UN = WT < 0 ? 1 : MODE == kFlagPass ? (WN >= 8 ? 1 : 8 / WN) : (WN <= 3 ? 2 : 1);
       for (int g0 = threadIdx.x; g0 < groups; g0 += UN * blockDim.x) {
         uint4 raw[UN][WN];
         float4 st[UN][6];
@@ -200,7 +206,8 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
           if (g < groups) {
             const int64_t off = (int64_t)g * 8, e = start + off;
 #pragma unroll
-            for (int h = 0; h < WN; ++h) raw[u][h] = zr::ld_once(gp[h] + off);
+            for (int h = 0; h < WN; ++h)
+              if (WT > 0 || h < W) raw[u][h] = zr::ld_once(gp[h] + off);
             if constexpr (kState) {
               st[u][0] = ld_state<MODE>(mst_in + e);
               st[u][1] = ld_state<MODE>(mst_in + e + 4);
@@ -219,10 +226,12 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
             zr::unpack8<DT>(raw[u][0], s);
 #pragma unroll
             for (int h = 1; h < WN; ++h) {
-              float x[8];
-              zr::unpack8<DT>(raw[u][h], x);
+              if (WT > 0 || h < W) {
+                float x[8];
+                zr::unpack8<DT>(raw[u][h], x);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x[j]);
+                for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x[j]);
+              }
             }
             if constexpr (kState) {
               bad |= update_group<DT>(a, K, out, start + (int64_t)g * 8, s, st[u][0], st[u][1], st[u][2], st[u][3],
@@ -235,9 +244,9 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
         }
       }
     } else if (WT == 0 && AT == 1 && GT == DT) {
-      // Any other W (5-7, 16, 32, 64 ...): the group's state loads, then the replicas in
-      // batches of kBatch whose loads are issued together, added in ring order as they
-      // arrive.
+      // W > 8: the group's state loads, then the replicas in batches of kBatch, double
+      // buffered: the next batch's loads are in flight while the current one is added in
+      // ring order, so a thread never waits on fewer than kBatch replica loads.
       constexpr int kBatch = 8;
       for (int g = threadIdx.x; g < groups; g += blockDim.x) {
         const int64_t e = start + (int64_t)g * 8;
@@ -250,9 +259,7 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
           st[4] = ld_state<MODE>(v_in + e);
           st[5] = ld_state<MODE>(v_in + e + 4);
         }
-        float s[8];
-        for (int h0 = 0; h0 < W; h0 += kBatch) {
-          uint4 raw[kBatch];
+        auto load_batch = [&](uint4(&raw)[kBatch], int h0) {
 #pragma unroll
           for (int j = 0; j < kBatch; ++j) {
             if (h0 + j < W) {
@@ -261,6 +268,9 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
               raw[j] = zr::ld_once(static_cast<const uint16_t*>(a.grads[a.order[pos]]) + e);
             }
           }
+        };
+        float s[8];
+        auto add_batch = [&](const uint4(&raw)[kBatch], int h0) {
 #pragma unroll
           for (int j = 0; j < kBatch; ++j) {
             if (h0 + j < W) {
@@ -270,6 +280,14 @@ __global__ void __launch_bounds__(kThreads, 2) fused_step_kernel(const __grid_co
               for (int k = 0; k < 8; ++k) s[k] = h0 + j == 0 ? x[k] : __fadd_rn(s[k], x[k]);
             }
           }
+        };
+        uint4 ra[kBatch], rb[kBatch];
+        load_batch(ra, 0);
+        for (int h0 = 0; h0 < W; h0 += 2 * kBatch) {
+          if (h0 + kBatch < W) load_batch(rb, h0 + kBatch);
+          add_batch(ra, h0);
+          if (h0 + 2 * kBatch < W) load_batch(ra, h0 + 2 * kBatch);
+          if (h0 + kBatch < W) add_batch(rb, h0 + kBatch);
         }
         if constexpr (kState) {
           bad |= update_group<DT>(a, K, out, e, s, st[0], st[1], st[2], st[3], st[4], st[5]);
@@ -376,7 +394,7 @@ KernelFn pick_kernel(int W, int A, bool fp32_grads) {
       case 3: return fused_step_kernel<DT, 3, 1, DT, MODE>;
       case 4: return fused_step_kernel<DT, 4, 1, DT, MODE>;
       case 8: return fused_step_kernel<DT, 8, 1, DT, MODE>;
-      default: return fused_step_kernel<DT, 0, 1, DT, MODE>;
+      default: return W < 8 ? fused_step_kernel<DT, -1, 1, DT, MODE> : fused_step_kernel<DT, 0, 1, DT, MODE>;
     }
   }
   if (A == 4) {
