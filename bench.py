@@ -67,14 +67,15 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def _traffic_record(workload: str, prefix: str = "fused_step", key: str = "traffic_bytes_per_launch"):
+def _traffic_record(workload: str, prefix: str = "fused_step", key: str = "traffic_bytes_per_launch",
+                    files=("zr_step_kernel.cuh", "zr_device.cuh")):
     """DRAM bytes of the fused kernel per launch (or of the in-place step's two launches, per step) from the
     committed ncu summary, if the kernel source has not changed since it was taken (the summary records the
-    source hash)."""
+    hash of the kernel's source files)."""
     import hashlib
     src = os.path.join(ROOT, "zero_gradient_reduction_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("zr_step_kernel.cuh", "zr_device.cuh"):
+    for f in files:
         with open(os.path.join(src, f), "rb") as fh:
             h.update(fh.read())
     digest = h.hexdigest()[:16]
@@ -434,6 +435,45 @@ def _measure_step(args, w, plan, hyper, state, grads, dev, stream, ws, gpu_index
             "roofline": roofline, "clocks": clk, "current": rep.current}
 
 
+def _measure_bulk(args, w, zr, plan, hyper, state, grads, dev, stream, steps=20):
+    """The same step with its loads staged in shared memory by bulk copies (zr_plan_set_staging(BULK), automatic
+    stage shape), captured as a CUDA graph and timed like the main step on the same buffers; register staging is
+    restored afterwards."""
+    import torch
+    if w.A != 1:
+        return None
+    try:
+        plan.set_staging(zr.STAGING_BULK)
+    except zr.ZrError as ex:
+        return {"unavailable": str(ex)}
+    for _ in range(3):
+        plan.step(grads, state, hyper, stream=stream)
+    torch.cuda.synchronize(dev)
+    g = plan.capture(grads, state, hyper)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    rep = plan.report(stream)
+    assert rep.overflow == 0, rep.as_dict()
+    plan.set_staging(zr.STAGING_REGISTERS)
+    del g
+    ms = e0.elapsed_time(e1) / steps
+    peak, _ = _peaks()
+    achieved = rep.bytes_alg / (ms * 1e-3) / 1e9
+    traffic, _ = _traffic_record(w.name, "fused_bulk", files=("zr_step_bulk.cuh", "zr_step_kernel.cuh",
+                                                              "zr_device.cuh"))
+    return {"ms_per_step": ms, "Gparams_per_s": plan.n_real / ms / 1e6, "hbm_GBs": achieved,
+            "frac_of_measured_copy": achieved / peak, "traffic": traffic, "steps": steps,
+            "call": "zr_step after zr_plan_set_staging(ZR_STAGING_BULK) (automatic stage shape), captured as a "
+                    "CUDA graph: one producer warp per block issues cp.async.bulk copies of each stage's W replica "
+                    "and master/m/v slices into a shared-memory ring, eight consumer warps compute"}
+
+
 def _measure_noalloc(zr, plan, hyper, state, grads, w, dev, stream, current, reps=10):
     """zr_step_noalloc (scratch in a static device array, nothing allocated) against zr_step on the same
     buffers, both launched eagerly, CUDA events on the launching stream. Every step here is clean, so the
@@ -529,6 +569,11 @@ def run_zr(args, w):
                    "launches_per_step": 2, "state_bytes_saved_GB": 14 * n / 1e9,
                    "call": "zr_step_inplace captured as a CUDA graph (flag pass, then the update in place)"}
         del g_ip, one
+
+    # the same step with bulk-copy staging of its loads
+    bulk = None
+    if not args.no_chain and not inplace_main:
+        bulk = _measure_bulk(args, w, zr, plan, hyper, state, grads, dev, stream)
 
     # comparison point: the same step as the unfused chain of standalone calls (reduce-scatter per bucket
     # into fp32 sums, flag pass + AdamW in place, cast/all-gather), (2W + 38) bytes per param
@@ -743,6 +788,7 @@ def run_zr(args, w):
         w2 = zrgen.workload(args.second)
         plan2, hyper2, state2, grads2 = _setup(w2, zr, zrgen, dev, stream, False)
         m2 = _measure_step(args, w2, plan2, hyper2, state2, grads2, dev, stream, ws, gpu_index, False)
+        bulk2 = _measure_bulk(args, w2, zr, plan2, hyper2, state2, grads2, dev, stream)
         noalloc = None
         try:
             noalloc = _measure_noalloc(zr, plan2, hyper2, state2, grads2, w2, dev, stream, m2["current"])
@@ -753,7 +799,8 @@ def run_zr(args, w):
                                     "per timed step"),
                   "value": m2["value"], "unit": "Gparams/s", "ms_per_step": m2["ms_step"], "steps": args.steps,
                   "warmup": args.warmup, "hbm_tbs": m2["achieved"] / 1e3, "roofline": m2["roofline"],
-                  "clocks": m2["clocks"], "gpu_launches": args.steps, "noalloc_step": noalloc}
+                  "clocks": m2["clocks"], "gpu_launches": args.steps, "bulk_staging": bulk2,
+                  "noalloc_step": noalloc}
         plan2.close()
         del plan2, state2, grads2
     else:
@@ -777,6 +824,7 @@ def run_zr(args, w):
         "unfused_chain": chain,
         "zero3_param_gather": zero3,
         "inplace_step": inplace,
+        "bulk_staging": bulk,
         "bucketed_overlap": overlap,
         "zero_offload": offload,
         "gpu_launches": args.steps * (2 if inplace_main else 1),

@@ -31,12 +31,14 @@ def _gpu():
     torch.cuda.empty_cache()
 
 
-def run_sampled(w: zrgen.Workload, steps=None, extra_buckets=3, inplace=False):
+def run_sampled(w: zrgen.Workload, steps=None, extra_buckets=3, inplace=False, staging=None):
     """Steps the workload and checks sampled windows against the oracle; inplace: one state set,
-    stepped with zr_step_inplace."""
+    stepped with zr_step_inplace; staging: zr_plan_set_staging's staging for zr_step."""
     steps = steps or w.steps
     plan = zr.Plan(list(w.tensors), W=w.W, A=w.A, dtype=w.dtype, stage=w.stage, cap=w.cap,
                    scaler=zr.Scaler(w.init_scale, w.dynamic))
+    if staging is not None:
+        plan.set_staging(staging)
     obuckets, ooffsets = oracle_layout(plan, w.tensors, w.cap, w.W)
     layout = Layout(w.tensors, ooffsets, zrgen.sigma_per_tensor(w), w.seed, w.dtype, w.master_sigma)
     cs = torch.cuda.current_stream().cuda_stream
@@ -112,6 +114,20 @@ def free_bytes() -> int:
 def test_gpt2_full_size():
     rep = run_sampled(zrgen.workload("gpt2"))
     assert rep.t == 10 and rep.n_real == 123_586_560
+
+
+def test_gpt2_full_size_bulk_staging():
+    rep = run_sampled(zrgen.workload("gpt2"), steps=3, staging=zr.STAGING_BULK)
+    assert rep.t == 3
+
+
+def test_7b_slice_bulk_staging_with_overflow_skip():
+    """One 200M-param bucket of the 7B workload's configuration (W = 2, fp16, dynamic scale), bulk-staged, with a
+    +inf injected at step 3 as the 7B workload does."""
+    import dataclasses
+    w = dataclasses.replace(zrgen.workload("7b_slice"), inject_step=3)
+    rep = run_sampled(w, staging=zr.STAGING_BULK)
+    assert rep.t == 5 and rep.scale == 32768.0 and rep.skipped_total == 1
 
 
 def test_1p3b_full_size():

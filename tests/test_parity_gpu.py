@@ -252,9 +252,11 @@ class FusedRun:
     """A fused-step run on the GPU with the full oracle beside it (small sizes)."""
 
     def __init__(self, numels, W, A, dtype, cap, S, dynamic=False, order=None, seed=0, sigma=None, stage=2,
-                 interval=1000):
+                 interval=1000, staging=None):
         self.plan = zr.Plan(numels, W=W, A=A, dtype=dtype, stage=stage, cap=cap, order=order,
                             scaler=zr.Scaler(S, dynamic, growth_interval=interval))
+        if staging is not None:  # (staging, stage_elems, stages) for zr_plan_set_staging
+            self.plan.set_staging(*staging)
         self.W, self.A, self.dtype, self.order = W, A, dtype, order
         self.obuckets, self.ooffsets = oracle_layout(self.plan, numels, cap, W)
         sig = np.full(len(numels), 1e-2, F32) if sigma is None else np.asarray(sigma, F32)
@@ -475,3 +477,67 @@ def test_checkpoint_resume_is_byte_identical():
     with pytest.raises(zr.ZrError):
         bad = zr.Checkpoint(2, 1.0, 0, 0, 0, 0, 1.0, 1.0)
         second.plan.restore(bad)
+
+
+# ----------------------------------------------------------------------------- bulk-copy staging
+@pytest.mark.parametrize("W,dtype,shape", [(1, zr.BF16, (0, 0)), (2, zr.F16, (0, 0)), (2, zr.BF16, (256, 2)),
+                                           (3, zr.F16, (0, 0)), (5, zr.BF16, (1024, 4)), (8, zr.BF16, (0, 0)),
+                                           (8, zr.F16, (4096, 1)), (16, zr.F16, (0, 0)), (64, zr.BF16, (0, 0))])
+def test_bulk_staging_bit_exact(W, dtype, shape):
+    """zr_step with its loads staged in shared memory by bulk copies gives the oracle's bytes: ragged buckets,
+    a ring order, automatic and explicit stage shapes (down to stages of 256 elements and a single stage)."""
+    rng = np.random.default_rng(W * 31 + dtype)
+    numels = [1000, 37, 5000, 8, 123_457, 64, 9_999, 3, 40_000]
+    order = [int(x) for x in rng.permutation(W)]
+    run = FusedRun(numels, W, 1, dtype, cap=20_000, S=8.0, order=order, seed=21,
+                   sigma=rng.uniform(1e-3, 1e-1, size=len(numels)), staging=(zr.STAGING_BULK,) + shape)
+    for s in range(1, 4):
+        run.step(s)
+        run.check(f"bulk W={W} shape={shape} step {s}: ")
+
+
+def test_bulk_staging_skip_and_scale():
+    """A +inf in one bucket skips the whole bulk-staged step and halves the dynamic scale, like the register
+    path; switching back to register staging between steps continues the same run."""
+    numels = [30_000, 4_000, 70_000]
+    run = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=5,
+                   staging=(zr.STAGING_BULK, 0, 0))
+    rep, orep = run.step(1)
+    assert rep.overflow == 0
+    before = [x.copy() for x in run.live()]
+    rep, orep = run.step(2, inject=(1, int(run.ooffsets[2]) + 123))
+    assert rep.overflow == 1 and rep.scale == 32768.0 and rep.t == 1
+    assert all(np.array_equal(a, b) for a, b in zip(before, run.live()))
+    run.check("after skip: ")
+    run.plan.set_staging(zr.STAGING_REGISTERS)
+    run.step(3)
+    run.check("register staging after bulk: ")
+    run.plan.set_staging(zr.STAGING_BULK)
+    run.step(4)
+    run.check("bulk staging again: ")
+
+
+def test_bulk_staging_large_plan_one_block_per_tile():
+    """A plan with more than four waves of 32K-element tiles: the bulk-staged step launches one block per
+    tile (the launch shape the benchmark times); sampled against the oracle on a window set."""
+    w = zrgen.workload("gpt2")
+    run = FusedRun(list(w.tensors)[:25], 8, 1, zr.BF16, cap=w.cap, S=1.0, seed=w.seed,
+                   staging=(zr.STAGING_BULK, 0, 0))
+    assert run.plan.numel > 4 * 152 * 2 * 32768
+    for s in (1, 2):
+        run.step(s)
+        run.check(f"large bulk step {s}: ")
+
+
+def test_bulk_staging_rejects_unsupported():
+    plan = zr.Plan([4096], W=2, A=4, dtype=zr.BF16, stage=2, cap=8192)
+    with pytest.raises(zr.ZrError):
+        plan.set_staging(zr.STAGING_BULK)
+    plan.close()
+    plan = zr.Plan([4096], W=2, A=1, dtype=zr.BF16, stage=2, cap=8192)
+    for bad in ((2, 0, 0), (zr.STAGING_BULK, 12, 0), (zr.STAGING_BULK, 0, 5)):
+        with pytest.raises(zr.ZrError):
+            plan.set_staging(*bad)
+    with pytest.raises(zr.ZrError):  # 4 stages of 65536 elements do not fit an SM
+        plan.set_staging(zr.STAGING_BULK, 65536, 4)
+    plan.close()

@@ -18,6 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libzr.so")
 
 F16, BF16, F32 = 0, 1, 2
+STAGING_REGISTERS, STAGING_BULK = 0, 1  # zr_staging
 MAX_W, MAX_REPLICAS, ALIGN = 64, 256, 8
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "out of memory", 5: "timeout"}
 
@@ -99,6 +100,7 @@ def lib():
                 "zr_accumulate": (st, [vp, i32, vp, i64, i32, vp]),
                 "zr_step_bucket": (st, [vp, i32, i32, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp]),
                 "zr_plan_set_bucket_blocks": (st, [vp, i32]),
+                "zr_plan_set_staging": (st, [vp, i32, i32, i32]),
                 "zr_offload_adamw": (st, [vp, vp, vp, vp, vp, i32, i64, ctypes.POINTER(Hyper), ctypes.c_float, i32,
                                           i64, i32, ctypes.POINTER(ctypes.c_int32)]),
                 "zr_offload_step": (st, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(Hyper),
@@ -447,6 +449,10 @@ class Plan:
         _check(lib().zr_step_bucket(self._h, int(stage if stage is not None else self.stage), int(bucket),
                                     ctypes.addressof(arr), ctypes.byref(st), ctypes.byref(h), _stream_handle(stream)))
 
+    def set_staging(self, staging: int, stage_elems: int = 0, stages: int = 0) -> None:
+        """zr_plan_set_staging: STAGING_REGISTERS (default) or STAGING_BULK for zr_step's loads."""
+        _check(lib().zr_plan_set_staging(self._h, int(staging), int(stage_elems), int(stages)))
+
     def set_bucket_blocks(self, max_blocks: int) -> None:
         """Cap every zr_step_bucket launch at max_blocks thread blocks (0: no cap), between steps."""
         _check(lib().zr_plan_set_bucket_blocks(self._h, int(max_blocks)))
@@ -565,4 +571,4 @@ def step_noalloc(buckets: np.ndarray, W: int, A: int, dtype: int, grads: Sequenc
 
 __all__ = ["lib", "ZrError", "chunk_size", "bucket_plan", "model_state_bytes", "ring_traffic", "reduce_scatter",
            "all_reduce", "adamw_shard_step", "accumulate", "offload_adamw", "all_gather", "AdamW", "Scaler",
-           "State", "State1", "Plan", "step_noalloc", "F16", "BF16", "F32"]
+           "State", "State1", "Plan", "step_noalloc", "F16", "BF16", "F32", "STAGING_REGISTERS", "STAGING_BULK"]

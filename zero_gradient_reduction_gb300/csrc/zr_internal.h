@@ -29,7 +29,8 @@ struct Ctrl {
   int64_t good, t, steps, skipped;
   double prod1, prod2;    // beta1^t, beta2^t (running products)
   int32_t offload_flag;   // overflow flag of the reduce-scatter in zr_offload_step
-  int32_t pad[3];         // to a multiple of 16 bytes: the step's epilogue moves it as 16-byte words
+  int32_t error;          // a bulk-staged step gave up a wait (the step was skipped); cleared by a reset
+  int32_t pad[2];         // to a multiple of 16 bytes: the step's epilogue moves it as 16-byte words
 };
 static_assert(sizeof(Ctrl) % 16 == 0, "Ctrl is read and written as 16-byte words");
 

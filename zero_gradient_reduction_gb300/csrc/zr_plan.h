@@ -23,6 +23,11 @@ struct zr_plan {
   void* kernel = nullptr;  // the fused_step_kernel instantiation for (dtype, W, A)
   int grid = 0;
   int64_t resident = 0;    // blocks of that kernel that fit on the GPU at once
+  // zr_step with its loads staged by bulk copies (zr_plan_set_staging): the kernel, its
+  // stage size and count, dynamic shared memory per block and grid
+  int staging = 0;         // ZR_STAGING_REGISTERS or ZR_STAGING_BULK
+  void* bulk_kernel = nullptr;
+  int bulk_E = 0, bulk_NS = 0, bulk_smem = 0, bulk_grid = 0;
   int device = 0;
   // bucketed launches (zr_step_bucket): bucket b's tiles are [tile_begin[b], tile_begin[b+1]),
   // launched with bucket_grid[b] blocks; a step's launches add up to bucket_blocks blocks

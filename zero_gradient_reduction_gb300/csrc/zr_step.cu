@@ -28,6 +28,7 @@ namespace zr {
 
 #include "zr_plan.h"
 #include "zr_step_kernel.cuh"
+#include "zr_step_bulk.cuh"
 
 namespace {
 
@@ -251,6 +252,9 @@ extern "C" zr_status zr_plan_report(zr_plan* p, void* stream, zr_step_report* re
   rep->good = c.good;
   rep->n_real = p->n_real;
   rep->bytes_alg = (int64_t)(2 * p->W * p->A + 26) * p->n_real;
+  if (c.error)
+    return fail(ZR_ERR_TIMEOUT, "zr_plan_report: a wait of the bulk-staged step gave up; that step was skipped "
+                "(state unchanged); zr_plan_reset clears the error");
   return ZR_OK;
 }
 
@@ -334,9 +338,68 @@ extern "C" zr_status zr_step(zr_plan* p, int stage, const void* const* grads, co
   zr_status s = check_step_args(p, stage, grads, st, h);
   if (s != ZR_OK) return s;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  s = launch_step(p, stage, grads, st, h, cs, 0, p->ntiles, p->grid, (unsigned)p->grid);
+  if (p->staging == ZR_STAGING_BULK && p->ntiles > 0) {
+    const FusedArgs a = make_args(p, stage, grads, st->master, st->m, st->v, st->param, h, 0, p->ntiles,
+                                  (unsigned)p->bulk_grid);
+    const BulkCfg cfg{p->bulk_E, p->bulk_NS};
+    reinterpret_cast<BulkKernelFn>(p->bulk_kernel)<<<p->bulk_grid, kBulkThreads, p->bulk_smem, cs>>>(a, cfg);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(ZR_ERR_CUDA, "zr_step: launch failed: %s", cudaGetErrorString(e));
+  } else {
+    s = launch_step(p, stage, grads, st, h, cs, 0, p->ntiles, p->grid, (unsigned)p->grid);
+  }
   if (s != ZR_OK || !rep) return s;
   return zr_plan_report(p, stream, rep);
+}
+
+extern "C" zr_status zr_plan_set_staging(zr_plan* p, int staging, int stage_elems, int stages) {
+  zr::clear_error();
+  if (!p) return fail(ZR_ERR_INVALID, "zr_plan_set_staging: null plan");
+  if (staging == ZR_STAGING_REGISTERS) {
+    p->staging = ZR_STAGING_REGISTERS;
+    return ZR_OK;
+  }
+  if (staging != ZR_STAGING_BULK) return fail(ZR_ERR_INVALID, "zr_plan_set_staging: unknown staging %d", staging);
+  if (p->A != 1 || p->fp32_grads)
+    return fail(ZR_ERR_UNSUPPORTED, "zr_plan_set_staging: bulk staging needs A = 1 and 16-bit gradients");
+  if (stage_elems < 0 || (stage_elems % 8) != 0 || stage_elems > 65536)
+    return fail(ZR_ERR_INVALID, "zr_plan_set_staging: stage_elems must be 0 or a multiple of 8 up to 65536");
+  if (stages < 0 || stages > kBulkMaxStages)
+    return fail(ZR_ERR_INVALID, "zr_plan_set_staging: stages must be 0 or 1..%d", kBulkMaxStages);
+  // Automatic shape: two blocks per SM (at most kBulkBudget of shared memory each), stages of
+  // 2048 elements (one 8-element group per consumer thread) where three of them fit, else
+  // smaller; as many stages as the budget holds, up to kBulkMaxStages.
+  constexpr int kBulkBudget = 110 * 1024;
+  int E = stage_elems, NS = stages;
+  if (E == 0) {
+    E = 2048;
+    while (E > 256 && 3 * bulk_stage_bytes(p->W, E) > kBulkBudget) E /= 2;
+  }
+  if (NS == 0) {
+    NS = kBulkBudget / bulk_stage_bytes(p->W, E);
+    NS = NS < 2 ? 2 : NS > kBulkMaxStages ? kBulkMaxStages : NS;
+  }
+  const int smem = NS * bulk_stage_bytes(p->W, E);
+  BulkKernelFn k = p->dtype == ZR_F16 ? pick_bulk_kernel<zr::DT_F16>(p->W) : pick_bulk_kernel<zr::DT_BF16>(p->W);
+  int per_sm = 0, sms = 0;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kBulkThreads, smem);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+  if (e != cudaSuccess) return cuda_fail("zr_plan_set_staging", e);
+  if (per_sm < 1)
+    return fail(ZR_ERR_UNSUPPORTED, "zr_plan_set_staging: %d stages of %d elements (%d bytes) do not fit an SM", NS, E,
+                smem);
+  const int64_t resident = (int64_t)sms * per_sm, nt = p->ntiles;
+  int grid = 1;
+  if (nt >= 4 * resident) grid = (int)(nt < (1 << 30) ? nt : (1 << 30));
+  else if (nt > 0) grid = (int)(nt < resident ? nt : resident);
+  p->bulk_kernel = reinterpret_cast<void*>(k);
+  p->bulk_E = E;
+  p->bulk_NS = NS;
+  p->bulk_smem = smem;
+  p->bulk_grid = grid;
+  p->staging = ZR_STAGING_BULK;
+  return ZR_OK;
 }
 
 extern "C" zr_status zr_step_bucket(zr_plan* p, int stage, int bucket, const void* const* grads, const zr_state* st,

@@ -13,7 +13,8 @@ from typing import List, Optional, Tuple
 
 import numpy as np
 
-__all__ = ["Workload", "WORKLOADS", "workload", "gpt2_small_tensors", "gpt_1p3b_tensors", "sweep_workloads",
+__all__ = ["Workload", "WORKLOADS", "workload", "width_workload", "gpt2_small_tensors", "gpt_1p3b_tensors",
+           "sweep_workloads",
            "sigma_per_tensor", "grad_scale", "inject_site"]
 
 
@@ -128,12 +129,22 @@ def sweep_workloads() -> List[Workload]:
     return out
 
 
+def width_workload(W: int) -> Workload:
+    """The GPT-2 shapes (123,586,560 params, 25M-param buckets, bf16) on W workers: cases a few GB in size for
+    widths with no workload of their own (W = 5, 6, 7, 16, 32, ...)."""
+    return Workload(f"gpt2_W{W}", tuple(_g2), W=W, A=1, dtype=1, stage=2, cap=25_000_000, steps=10, seed=0,
+                    sigma=None, init_scale=1.0, dynamic=False,
+                    description=f"GPT-2-small shapes, 123,586,560 params, W={W}, bf16, 25M-param buckets")
+
+
 def workload(name: str) -> Workload:
     if name in WORKLOADS:
         return WORKLOADS[name]
     for w in sweep_workloads():
         if w.name == name:
             return w
+    if name.startswith("gpt2_W") and name[6:].isdigit() and 1 <= int(name[6:]) <= 64:
+        return width_workload(int(name[6:]))
     raise KeyError(name)
 
 
