@@ -151,11 +151,12 @@ zr_status zr_accumulate(const void* grad, zr_dtype dt, float* acc, int64_t n, in
  *   g = sums * r,  r = fp32(1 / (loss_scale * W)) formed in double
  *   m = b1*m + (1-b1)*g ;  v = b2*v + (1-b2)*(g*g)
  *   u = (m / bc1) / (sqrt(v / bc2) + eps),  bc_i = fp32(1 - beta_i^t), beta_i^t a
- *       running product of t double multiplications
+ *       running product of t double multiplications (walked on the host only until it
+ *       stops changing, which for 0 <= beta < 1 it does within about 745/(1-beta) steps)
  *   master = master*(1 - lr*wd) - lr*u     (1-b1, 1-b2, 1-lr*wd formed in fp32)
  * t: the 1-based index of this update. All arrays: device fp32, len elements.
  * Errors: ZR_ERR_INVALID for len < 0, t < 1, W < 1, loss_scale <= 0 or not finite,
- * null h, null or misaligned pointers. len == 0 only runs nothing. */
+ * betas outside [0, 1), null h, null or misaligned pointers. len == 0 only runs nothing. */
 zr_status zr_adamw_shard_step(const float* shard_sums, float* m, float* v, float* master, int64_t len,
                               const zr_adamw_hyper* h, float loss_scale, int W, int64_t t,
                               int32_t* overflow, void* stream);
@@ -410,7 +411,7 @@ zr_status zr_gather_params(zr_plan* p, int bucket_lo, int bucket_hi, const void*
  * values of dt (may be NULL to skip the cast); nthreads worker threads (1..256).
  * If any sums value is not finite, *overflow = 1 and nothing is written; otherwise
  * *overflow = 0. Errors: ZR_ERR_INVALID for bad sizes, null pointers, dt, t < 1,
- * W < 1, a bad loss_scale. */
+ * W < 1, a bad loss_scale, betas outside [0, 1). */
 zr_status zr_offload_adamw(const float* sums, float* master, float* m, float* v, void* param16, zr_dtype dt,
                            int64_t n, const zr_adamw_hyper* h, float loss_scale, int W, int64_t t, int nthreads,
                            int32_t* overflow);
@@ -424,8 +425,8 @@ zr_status zr_offload_adamw(const float* sums, float* master, float* m, float* v,
  * b overlaps the copies of the other buckets. The last parameter copies are still
  * queued on `stream` at return: synchronise it before reading param_dev or reusing
  * param_host. The caller applies its loss-scale rule from *overflow (host int32).
- * Errors: ZR_ERR_INVALID for null or misaligned buffers, stage, t < 1;
- * ZR_ERR_UNSUPPORTED for A > 1; ZR_ERR_CUDA. */
+ * Errors: ZR_ERR_INVALID for null or misaligned buffers, stage, t < 1, betas outside
+ * [0, 1); ZR_ERR_UNSUPPORTED for A > 1; ZR_ERR_CUDA. */
 zr_status zr_offload_step(zr_plan* p, int stage, const void* const* grads, float* sums_dev, float* sums_host,
                           float* master, float* m, float* v, void* param_host, void* param_dev,
                           const zr_adamw_hyper* h, float loss_scale, int64_t t, int nthreads, void* stream,
@@ -455,9 +456,13 @@ zr_status zr_offload_step(zr_plan* p, int stage, const void* const* grads, float
  * array of device pointers, replica w*A + a, each covering every bucket. order: ring
  * order (NULL = identity). st/current: reads state set `current`, writes set
  * 1-current in full. loss_scale and t (1-based index of this update) as in
- * zr_adamw_shard_step. overflow: device int32, set to 1 if any reduced gradient is
- * not finite, else 0; when it is 1 the written set must be discarded (keep
- * `current`), and the caller applies its own loss-scale rule.
+ * zr_adamw_shard_step; the bias corrections come from the same running products of the
+ * betas that zr_step keeps (fp32(1 - beta^t), beta^t as t double multiplications), which
+ * the library caches between calls, so stepping t = 1, 2, 3, ... costs one multiplication
+ * per call and any t costs at most the walk to the products' fixed point. overflow:
+ * device int32, set to 1 if any reduced gradient is not finite, else 0 (also 0 for an
+ * empty bucket table); when it is 1 the written set must be discarded (keep `current`),
+ * and the caller applies its own loss-scale rule.
  * The caller carries the live-set index, the scale and t between calls.
  *
  * Every call on a device reuses the same scratch and leaves its last contents there;
@@ -466,7 +471,7 @@ zr_status zr_offload_step(zr_plan* p, int stage, const void* const* grads, float
  * otherwise serialise them). The first call on a device looks up the scratch's device
  * address (cudaGetSymbolAddress); make it before any stream capture.
  * Errors: ZR_ERR_INVALID for the cases of zr_step, a bucket that breaks the ring rule,
- * current not 0/1, t < 1, a bad loss_scale, or buckets needing more than
+ * current not 0/1, t < 1, a bad loss_scale, betas outside [0, 1), or buckets needing more than
  * ZR_NOALLOC_MAX_TILES tiles (use zr_plan_create/zr_step for those); ZR_ERR_CUDA. */
 zr_status zr_step_noalloc(const zr_bucket* buckets, int nbuckets, int W, int A, zr_dtype dtype, const int* order,
                           const void* const* grads, const zr_state* st, int current, const zr_adamw_hyper* h,

@@ -541,3 +541,8 @@ def test_bulk_staging_rejects_unsupported():
     with pytest.raises(zr.ZrError):  # 4 stages of 65536 elements do not fit an SM
         plan.set_staging(zr.STAGING_BULK, 65536, 4)
     plan.close()
+    # a refused call leaves no CUDA error behind for the caller's next check
+    x = torch.empty(1024, device="cuda")
+    x.fill_(1.0)
+    torch.cuda.synchronize()
+    assert float(x.sum()) == 1024.0

@@ -16,6 +16,9 @@ zr_status fail(zr_status s, const char* fmt, ...) {
   va_start(ap, fmt);
   std::vsnprintf(g_err, sizeof g_err, fmt, ap);
   va_end(ap);
+  // a failed CUDA runtime call also leaves its code in the runtime's per-thread last
+  // error, where the caller's next unrelated check would find it: it is reported here
+  if (s == ZR_ERR_CUDA || s == ZR_ERR_OOM) take_cuda_error();
   return s;
 }
 

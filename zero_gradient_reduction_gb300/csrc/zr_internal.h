@@ -7,8 +7,10 @@
 
 namespace zr {
 
-// Thread-local last-error message; returns `s` for tail calls.
+// Thread-local last-error message; returns `s` for tail calls. For ZR_ERR_CUDA and
+// ZR_ERR_OOM it also clears the CUDA runtime's last error (take_cuda_error).
 zr_status fail(zr_status s, const char* fmt, ...);
+void take_cuda_error();
 void clear_error();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

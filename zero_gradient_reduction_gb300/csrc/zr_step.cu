@@ -24,7 +24,8 @@
 using zr::fail;
 
 namespace zr {
-}
+void take_cuda_error() { (void)cudaGetLastError(); }
+}  // namespace zr
 
 #include "zr_plan.h"
 #include "zr_step_kernel.cuh"
@@ -379,10 +380,17 @@ extern "C" zr_status zr_plan_set_staging(zr_plan* p, int staging, int stage_elem
     NS = kBulkBudget / bulk_stage_bytes(p->W, E);
     NS = NS < 2 ? 2 : NS > kBulkMaxStages ? kBulkMaxStages : NS;
   }
-  const int smem = NS * bulk_stage_bytes(p->W, E);
+  const int64_t smem64 = (int64_t)NS * bulk_stage_bytes(p->W, E);
+  int optin = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
+  if (e != cudaSuccess) return cuda_fail("zr_plan_set_staging", e);
+  if (smem64 > optin)
+    return fail(ZR_ERR_UNSUPPORTED, "zr_plan_set_staging: %d stages of %d elements need %lld bytes of shared memory "
+                "(a block may have %d)", NS, E, (long long)smem64, optin);
+  const int smem = (int)smem64;
   BulkKernelFn k = p->dtype == ZR_F16 ? pick_bulk_kernel<zr::DT_F16>(p->W) : pick_bulk_kernel<zr::DT_BF16>(p->W);
   int per_sm = 0, sms = 0;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kBulkThreads, smem);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
   if (e != cudaSuccess) return cuda_fail("zr_plan_set_staging", e);
