@@ -366,7 +366,7 @@ def _setup(w, zr, zrgen, dev, stream, inplace_main):
     return plan, hyper, state, grads
 
 
-def _measure_step(args, w, plan, hyper, state, grads, dev, stream, ws, gpu_index, inplace_main):
+def _measure_step(args, w, zr, plan, hyper, state, grads, dev, stream, ws, gpu_index, inplace_main):
     """The timed region: args.steps replays of the step captured as a CUDA graph, CUDA events on the launching
     stream, clocks sampled throughout; re-taken once if a thermal or hardware slowdown was seen. Returns the
     numbers of the JSON line for this workload."""
@@ -420,32 +420,50 @@ def _measure_step(args, w, plan, hyper, state, grads, dev, stream, ws, gpu_index
     peak, peak_kind = _peaks()
     step_bytes = rep.bytes_alg + (2 * w.W * w.A * plan.n_real if inplace_main else 0)
     achieved = step_bytes / (ms_total / args.steps * 1e-3) / 1e9
+    staging = _staging_name(zr, plan)
     if inplace_main:
         traffic, _digest = _traffic_record(w.name, "inplace_step", "traffic_bytes_per_step")
+        kernel = ("fused_step_kernel flag pass + in-place update (bytes and time of the step's two launches "
+                  "together)")
+    elif staging == "bulk":
+        traffic, _digest = _traffic_record(w.name, "fused_bulk", files=KERNEL_FILES["bulk"])
+        kernel = "fused_bulk_kernel (one launch per step; loads staged by cp.async.bulk into shared memory)"
     else:
         traffic, _digest = _traffic_record(w.name)
+        kernel = "fused_step_kernel (one launch per step; loads staged in registers)"
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "peak_source": f"{peak_kind} HBM copy bandwidth",
-                "frac_of_8tbs_nominal": achieved / 8000.0,
-                "kernel": "fused_step_kernel flag pass + in-place update (bytes and time of the step's two "
-                          "launches together)" if inplace_main else "fused_step_kernel (one launch per step)"}
+                "frac_of_8tbs_nominal": achieved / 8000.0, "kernel": kernel}
     clk = {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"), "reasons": clocks.get("reasons"),
            "samples": clocks.get("samples"), "power_w_max": clocks.get("power_w_max"), "attempts": attempts}
     return {"ms_step": ms_step, "value": value, "step_bytes": step_bytes, "achieved": achieved,
-            "roofline": roofline, "clocks": clk, "current": rep.current}
+            "roofline": roofline, "clocks": clk, "current": rep.current,
+            "staging": "one state set in place (register staging)" if inplace_main else staging}
 
 
-def _measure_bulk(args, w, zr, plan, hyper, state, grads, dev, stream, steps=20):
-    """The same step with its loads staged in shared memory by bulk copies (zr_plan_set_staging(BULK), automatic
-    stage shape), captured as a CUDA graph and timed like the main step on the same buffers; register staging is
-    restored afterwards."""
+# the fused kernels' source files, whose hash a committed traffic record must match
+KERNEL_FILES = {"registers": ("zr_step_kernel.cuh", "zr_device.cuh"),
+                "bulk": ("zr_step_bulk.cuh", "zr_step_kernel.cuh", "zr_device.cuh")}
+
+
+def _staging_name(zr, plan) -> str:
+    return "bulk" if plan.staging == zr.STAGING_BULK else "registers"
+
+
+def _measure_other_staging(args, w, zr, plan, hyper, state, grads, dev, stream, steps=20):
+    """The same step with the other load staging than the plan's (bulk copies into shared memory, or 16-byte loads
+    into registers), captured as a CUDA graph and timed like the main step on the same buffers; the plan's own
+    staging is restored afterwards."""
     import torch
     if w.A != 1:
         return None
+    own = plan.staging
+    other = zr.STAGING_REGISTERS if own == zr.STAGING_BULK else zr.STAGING_BULK
     try:
-        plan.set_staging(zr.STAGING_BULK)
+        plan.set_staging(other)
     except zr.ZrError as ex:
         return {"unavailable": str(ex)}
+    name = _staging_name(zr, plan)
     for _ in range(3):
         plan.step(grads, state, hyper, stream=stream)
     torch.cuda.synchronize(dev)
@@ -460,18 +478,15 @@ def _measure_bulk(args, w, zr, plan, hyper, state, grads, dev, stream, steps=20)
     torch.cuda.synchronize(dev)
     rep = plan.report(stream)
     assert rep.overflow == 0, rep.as_dict()
-    plan.set_staging(zr.STAGING_REGISTERS)
+    plan.set_staging(own)
     del g
     ms = e0.elapsed_time(e1) / steps
     peak, _ = _peaks()
     achieved = rep.bytes_alg / (ms * 1e-3) / 1e9
-    traffic, _ = _traffic_record(w.name, "fused_bulk", files=("zr_step_bulk.cuh", "zr_step_kernel.cuh",
-                                                              "zr_device.cuh"))
-    return {"ms_per_step": ms, "Gparams_per_s": plan.n_real / ms / 1e6, "hbm_GBs": achieved,
+    traffic, _ = _traffic_record(w.name, "fused_bulk" if name == "bulk" else "fused_step", files=KERNEL_FILES[name])
+    return {"staging": name, "ms_per_step": ms, "Gparams_per_s": plan.n_real / ms / 1e6, "hbm_GBs": achieved,
             "frac_of_measured_copy": achieved / peak, "traffic": traffic, "steps": steps,
-            "call": "zr_step after zr_plan_set_staging(ZR_STAGING_BULK) (automatic stage shape), captured as a "
-                    "CUDA graph: one producer warp per block issues cp.async.bulk copies of each stage's W replica "
-                    "and master/m/v slices into a shared-memory ring, eight consumer warps compute"}
+            "call": "zr_step after zr_plan_set_staging to the other staging, captured as a CUDA graph"}
 
 
 def _measure_noalloc(zr, plan, hyper, state, grads, w, dev, stream, current, reps=10):
@@ -535,8 +550,10 @@ def run_zr(args, w):
     stream = torch.cuda.current_stream(dev)
     inplace_main = args.inplace or w.state_sets == 1
     plan, hyper, state, grads = _setup(w, zr, zrgen, dev, stream, inplace_main)
+    if args.staging:
+        plan.set_staging(zr.STAGING_BULK if args.staging == "bulk" else zr.STAGING_REGISTERS)
     n = plan.numel
-    main = _measure_step(args, w, plan, hyper, state, grads, dev, stream, ws, gpu_index, inplace_main)
+    main = _measure_step(args, w, zr, plan, hyper, state, grads, dev, stream, ws, gpu_index, inplace_main)
     ms_step, value, step_bytes = main["ms_step"], main["value"], main["step_bytes"]
     peak, _ = _peaks()
     rep = plan.report(stream)
@@ -570,10 +587,10 @@ def run_zr(args, w):
                    "call": "zr_step_inplace captured as a CUDA graph (flag pass, then the update in place)"}
         del g_ip, one
 
-    # the same step with bulk-copy staging of its loads
-    bulk = None
+    # the same step with the other load staging (register loads, or bulk copies into shared memory)
+    other = None
     if not args.no_chain and not inplace_main:
-        bulk = _measure_bulk(args, w, zr, plan, hyper, state, grads, dev, stream)
+        other = _measure_other_staging(args, w, zr, plan, hyper, state, grads, dev, stream)
 
     # comparison point: the same step as the unfused chain of standalone calls (reduce-scatter per bucket
     # into fp32 sums, flag pass + AdamW in place, cast/all-gather), (2W + 38) bytes per param
@@ -787,19 +804,19 @@ def run_zr(args, w):
         torch.cuda.empty_cache()
         w2 = zrgen.workload(args.second)
         plan2, hyper2, state2, grads2 = _setup(w2, zr, zrgen, dev, stream, False)
-        m2 = _measure_step(args, w2, plan2, hyper2, state2, grads2, dev, stream, ws, gpu_index, False)
-        bulk2 = _measure_bulk(args, w2, zr, plan2, hyper2, state2, grads2, dev, stream)
+        m2 = _measure_step(args, w2, zr, plan2, hyper2, state2, grads2, dev, stream, ws, gpu_index, False)
+        other2 = _measure_other_staging(args, w2, zr, plan2, hyper2, state2, grads2, dev, stream)
         noalloc = None
         try:
             noalloc = _measure_noalloc(zr, plan2, hyper2, state2, grads2, w2, dev, stream, m2["current"])
         except Exception as ex:  # a workload beyond the static scratch is refused by the call itself
             noalloc = {"unavailable": str(ex).splitlines()[0]}
-        second = {"config": _config(w2, plan2.buckets, f"inputs larger than L2: {m2['step_bytes'] / 1e9:.1f} GB "
-                                    "moved per step", launch="zr_step captured once as a CUDA graph, replayed once "
-                                    "per timed step"),
+        second = {"config": dict(_config(w2, plan2.buckets, f"inputs larger than L2: {m2['step_bytes'] / 1e9:.1f} GB "
+                                         "moved per step", launch="zr_step captured once as a CUDA graph, replayed "
+                                         "once per timed step"), staging=m2["staging"]),
                   "value": m2["value"], "unit": "Gparams/s", "ms_per_step": m2["ms_step"], "steps": args.steps,
                   "warmup": args.warmup, "hbm_tbs": m2["achieved"] / 1e3, "roofline": m2["roofline"],
-                  "clocks": m2["clocks"], "gpu_launches": args.steps, "bulk_staging": bulk2,
+                  "clocks": m2["clocks"], "gpu_launches": args.steps, "other_staging": other2,
                   "noalloc_step": noalloc}
         plan2.close()
         del plan2, state2, grads2
@@ -819,12 +836,13 @@ def run_zr(args, w):
                           "zr_step captured once as a CUDA graph, replayed once per timed step", inplace=inplace_main),
         "hbm_tbs": main["achieved"] / 1e3,
         "roofline": main["roofline"],
+        "staging": main["staging"],
         "cpu_baseline": cpu,
         "e2e": e2e,
         "unfused_chain": chain,
         "zero3_param_gather": zero3,
         "inplace_step": inplace,
-        "bulk_staging": bulk,
+        "other_staging": other,
         "bucketed_overlap": overlap,
         "zero_offload": offload,
         "gpu_launches": args.steps * (2 if inplace_main else 1),
@@ -856,6 +874,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chain", action="store_true")
     ap.add_argument("--chain-steps", type=int, default=5)
+    ap.add_argument("--staging", choices=["bulk", "registers"], default=None,
+                    help="load staging of the main step's zr_step (default: the plan's own choice)")
     ap.add_argument("--inplace", action="store_true",
                     help="time zr_step_inplace on one state set as the main step (always so for 13b)")
     args = ap.parse_args()

@@ -287,14 +287,15 @@ zr_status zr_step_bucket(zr_plan* p, int stage, int bucket, const void* const* g
  * blocks of all its launches). Errors: ZR_ERR_INVALID for a null plan or max_blocks < 0. */
 zr_status zr_plan_set_bucket_blocks(zr_plan* p, int max_blocks);
 
-/* How zr_step moves a tile's inputs into the SMs. ZR_STAGING_REGISTERS (the default):
- * every thread issues its 16-byte loads of the W replicas and of master/m/v into registers
- * before any arithmetic. ZR_STAGING_BULK: a producer warp per block copies each stage of a
- * tile (stage_elems elements of the W replicas and of master/m/v) into shared memory with
+/* How zr_step moves a tile's inputs into the SMs. ZR_STAGING_REGISTERS: every thread
+ * issues its 16-byte loads of the W replicas and of master/m/v into registers before any
+ * arithmetic. ZR_STAGING_BULK: a producer warp per block copies each stage of a tile
+ * (stage_elems elements of the W replicas and of master/m/v) into shared memory with
  * one-dimensional bulk copies (cp.async.bulk, this GPU's memory only) completed on mbarriers,
  * keeping `stages` stages in flight, and eight consumer warps compute from shared memory.
  * Both give the same bytes; only speed differs. Bulk staging covers zr_step (and its CUDA
- * graph capture) for plans with A = 1 and 16-bit gradients; the other calls keep register
+ * graph capture) for plans with A = 1 and 16-bit gradients, and is what zr_plan_create
+ * chooses for them (automatic shape); other plans, and the other calls, use register
  * staging. stage_elems = 0 and stages = 0 choose a shape that lets two blocks share an SM.
  * Every wait of a bulk-staged step is bounded (2 s); one that gives up skips the step and
  * makes zr_plan_report (and zr_step with a report) return ZR_ERR_TIMEOUT until
@@ -303,6 +304,8 @@ zr_status zr_plan_set_bucket_blocks(zr_plan* p, int max_blocks);
  * shape that does not fit an SM's shared memory), ZR_ERR_CUDA. */
 typedef enum { ZR_STAGING_REGISTERS = 0, ZR_STAGING_BULK = 1 } zr_staging;
 zr_status zr_plan_set_staging(zr_plan* p, int staging, int stage_elems, int stages);
+/* The staging zr_step uses for plan p (a zr_staging value); -1 for a null plan. */
+int zr_plan_staging(const zr_plan* p);
 
 /* The optimizer state and the parameter replica as ONE set (zr_step_inplace). Device
  * pointers, zr_plan_numel elements each; param is of the plan's dtype. */

@@ -44,8 +44,9 @@ def test_random_plan_matches_oracle(case):
     dynamic = bool(rng.integers(0, 2))
     sigma = rng.uniform(1e-3, 1e-1, size=ntensors)
     cls = InPlaceRun if rng.integers(0, 2) else FusedRun
+    staging = None if rng.integers(0, 2) else (zr.STAGING_REGISTERS, 0, 0)  # the plan's own (bulk if A = 1)
     run = cls(numels, W, A, dtype, cap=cap, S=S, dynamic=dynamic, order=order, seed=case, sigma=sigma,
-              interval=2)
+              interval=2, staging=staging)
     where = f"case {case}: W={W} A={A} dtype={dtype} cap={cap} numels={numels} {cls.__name__}"
     for s in (1, 2, 3):
         run.step(s)

@@ -116,9 +116,14 @@ def test_gpt2_full_size():
     assert rep.t == 10 and rep.n_real == 123_586_560
 
 
-def test_gpt2_full_size_bulk_staging():
-    rep = run_sampled(zrgen.workload("gpt2"), steps=3, staging=zr.STAGING_BULK)
+def test_gpt2_full_size_register_staging():
+    rep = run_sampled(zrgen.workload("gpt2"), steps=3, staging=zr.STAGING_REGISTERS)
     assert rep.t == 3
+
+
+def test_1p3b_full_size_register_staging():
+    rep = run_sampled(zrgen.workload("1p3b"), steps=2, staging=zr.STAGING_REGISTERS)
+    assert rep.t == 2
 
 
 def test_7b_slice_bulk_staging_with_overflow_skip():

@@ -308,11 +308,15 @@ class FusedRun:
         assert_state_close(*self.live(), *self.o, exact=True, where=where)
 
 
-def test_fused_tiny_config_bit_exact():
-    """flat n = 786,432, W = 3, fp16, one bucket, S = 1024 static, 3 steps, seed 0."""
+@pytest.mark.parametrize("staging", [None, zr.STAGING_REGISTERS])
+def test_fused_tiny_config_bit_exact(staging):
+    """flat n = 786,432, W = 3, fp16, one bucket, S = 1024 static, 3 steps, seed 0; the plan's own staging
+    (bulk copies) and register staging."""
     w = zrgen.workload("tiny")
     run = FusedRun(list(w.tensors), w.W, w.A, w.dtype, w.cap, w.init_scale, w.dynamic, seed=w.seed,
-                   sigma=zrgen.sigma_per_tensor(w), stage=w.stage)
+                   sigma=zrgen.sigma_per_tensor(w), stage=w.stage,
+                   staging=None if staging is None else (staging, 0, 0))
+    assert run.plan.staging == (zr.STAGING_BULK if staging is None else staging)
     assert len(run.plan.buckets) == 1 and run.plan.numel == 786_432
     for s in range(1, w.steps + 1):
         rep, orep = run.step(s)
@@ -324,12 +328,17 @@ def test_fused_tiny_config_bit_exact():
                                        (7, 1, zr.F16), (8, 1, zr.BF16), (2, 4, zr.BF16), (4, 4, zr.F16),
                                        (8, 4, zr.BF16), (3, 3, zr.BF16), (9, 1, zr.BF16), (16, 1, zr.F16),
                                        (17, 1, zr.BF16), (24, 1, zr.F16), (33, 1, zr.BF16)])
-def test_fused_ragged_buckets(W, A, dtype):
+@pytest.mark.parametrize("staging", [None, zr.STAGING_REGISTERS])
+def test_fused_ragged_buckets(W, A, dtype, staging):
+    if A > 1 and staging is not None:
+        pytest.skip("plans with A > 1 always use register staging")
     rng = np.random.default_rng(W * 100 + A)
     numels = [1000, 37, 5000, 8, 123_457, 64, 9_999, 3, 40_000]
     order = list(rng.permutation(W))
     run = FusedRun(numels, W, A, dtype, cap=20_000, S=8.0, order=order, seed=3,
-                   sigma=rng.uniform(1e-3, 1e-1, size=len(numels)))
+                   sigma=rng.uniform(1e-3, 1e-1, size=len(numels)),
+                   staging=None if staging is None else (staging, 0, 0))
+    assert run.plan.staging == (zr.STAGING_BULK if staging is None and A == 1 else zr.STAGING_REGISTERS)
     assert len(run.plan.buckets) >= 4
     for s in range(1, 4):
         run.step(s)

@@ -101,6 +101,7 @@ def lib():
                 "zr_step_bucket": (st, [vp, i32, i32, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp]),
                 "zr_plan_set_bucket_blocks": (st, [vp, i32]),
                 "zr_plan_set_staging": (st, [vp, i32, i32, i32]),
+                "zr_plan_staging": (i32, [vp]),
                 "zr_offload_adamw": (st, [vp, vp, vp, vp, vp, i32, i64, ctypes.POINTER(Hyper), ctypes.c_float, i32,
                                           i64, i32, ctypes.POINTER(ctypes.c_int32)]),
                 "zr_offload_step": (st, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(Hyper),
@@ -450,8 +451,13 @@ class Plan:
                                     ctypes.addressof(arr), ctypes.byref(st), ctypes.byref(h), _stream_handle(stream)))
 
     def set_staging(self, staging: int, stage_elems: int = 0, stages: int = 0) -> None:
-        """zr_plan_set_staging: STAGING_REGISTERS (default) or STAGING_BULK for zr_step's loads."""
+        """zr_plan_set_staging: STAGING_BULK (the default where it applies) or STAGING_REGISTERS."""
         _check(lib().zr_plan_set_staging(self._h, int(staging), int(stage_elems), int(stages)))
+
+    @property
+    def staging(self) -> int:
+        """The staging zr_step uses for this plan (zr_plan_staging)."""
+        return int(lib().zr_plan_staging(self._h))
 
     def set_bucket_blocks(self, max_blocks: int) -> None:
         """Cap every zr_step_bucket launch at max_blocks thread blocks (0: no cap), between steps."""
