@@ -126,6 +126,11 @@ def test_1p3b_full_size_register_staging():
     assert rep.t == 2
 
 
+def test_gpt2_full_size_bulk_io_staging():
+    rep = run_sampled(zrgen.workload("gpt2"), steps=3, staging=zr.STAGING_BULK_IO)
+    assert rep.t == 3
+
+
 def test_7b_slice_bulk_staging_with_overflow_skip():
     """One 200M-param bucket of the 7B workload's configuration (W = 2, fp16, dynamic scale), bulk-staged, with a
     +inf injected at step 3 as the 7B workload does."""

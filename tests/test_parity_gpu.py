@@ -308,15 +308,16 @@ class FusedRun:
         assert_state_close(*self.live(), *self.o, exact=True, where=where)
 
 
-@pytest.mark.parametrize("staging", [None, zr.STAGING_REGISTERS])
+@pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
 def test_fused_tiny_config_bit_exact(staging):
     """flat n = 786,432, W = 3, fp16, one bucket, S = 1024 static, 3 steps, seed 0; the plan's own staging
-    (bulk copies) and register staging."""
+    (registers, for a plan this small) and bulk-copy staging."""
     w = zrgen.workload("tiny")
     run = FusedRun(list(w.tensors), w.W, w.A, w.dtype, w.cap, w.init_scale, w.dynamic, seed=w.seed,
                    sigma=zrgen.sigma_per_tensor(w), stage=w.stage,
                    staging=None if staging is None else (staging, 0, 0))
-    assert run.plan.staging == (zr.STAGING_BULK if staging is None else staging)
+    # a plan this small (launch-bound, L2-resident) keeps register staging by default
+    assert run.plan.staging == (zr.STAGING_REGISTERS if staging is None else staging)
     assert len(run.plan.buckets) == 1 and run.plan.numel == 786_432
     for s in range(1, w.steps + 1):
         rep, orep = run.step(s)
@@ -328,17 +329,18 @@ def test_fused_tiny_config_bit_exact(staging):
                                        (7, 1, zr.F16), (8, 1, zr.BF16), (2, 4, zr.BF16), (4, 4, zr.F16),
                                        (8, 4, zr.BF16), (3, 3, zr.BF16), (9, 1, zr.BF16), (16, 1, zr.F16),
                                        (17, 1, zr.BF16), (24, 1, zr.F16), (33, 1, zr.BF16)])
-@pytest.mark.parametrize("staging", [None, zr.STAGING_REGISTERS])
+@pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
 def test_fused_ragged_buckets(W, A, dtype, staging):
     if A > 1 and staging is not None:
-        pytest.skip("plans with A > 1 always use register staging")
+        pytest.skip("bulk staging covers A = 1 only")
     rng = np.random.default_rng(W * 100 + A)
     numels = [1000, 37, 5000, 8, 123_457, 64, 9_999, 3, 40_000]
     order = list(rng.permutation(W))
     run = FusedRun(numels, W, A, dtype, cap=20_000, S=8.0, order=order, seed=3,
                    sigma=rng.uniform(1e-3, 1e-1, size=len(numels)),
                    staging=None if staging is None else (staging, 0, 0))
-    assert run.plan.staging == (zr.STAGING_BULK if staging is None and A == 1 else zr.STAGING_REGISTERS)
+    # small plans keep register staging by default
+    assert run.plan.staging == (zr.STAGING_REGISTERS if staging is None else staging)
     assert len(run.plan.buckets) >= 4
     for s in range(1, 4):
         run.step(s)
@@ -492,25 +494,28 @@ def test_checkpoint_resume_is_byte_identical():
 @pytest.mark.parametrize("W,dtype,shape", [(1, zr.BF16, (0, 0)), (2, zr.F16, (0, 0)), (2, zr.BF16, (256, 2)),
                                            (3, zr.F16, (0, 0)), (5, zr.BF16, (1024, 4)), (8, zr.BF16, (0, 0)),
                                            (8, zr.F16, (4096, 1)), (16, zr.F16, (0, 0)), (64, zr.BF16, (0, 0))])
-def test_bulk_staging_bit_exact(W, dtype, shape):
-    """zr_step with its loads staged in shared memory by bulk copies gives the oracle's bytes: ragged buckets,
-    a ring order, automatic and explicit stage shapes (down to stages of 256 elements and a single stage)."""
+@pytest.mark.parametrize("mode", [zr.STAGING_BULK, zr.STAGING_BULK_IO])
+def test_bulk_staging_bit_exact(W, dtype, shape, mode):
+    """zr_step with its loads (and with BULK_IO its results too) staged in shared memory by bulk copies gives
+    the oracle's bytes: ragged buckets, a ring order, automatic and explicit stage shapes (down to stages of
+    256 elements and a single stage)."""
     rng = np.random.default_rng(W * 31 + dtype)
     numels = [1000, 37, 5000, 8, 123_457, 64, 9_999, 3, 40_000]
     order = [int(x) for x in rng.permutation(W)]
     run = FusedRun(numels, W, 1, dtype, cap=20_000, S=8.0, order=order, seed=21,
-                   sigma=rng.uniform(1e-3, 1e-1, size=len(numels)), staging=(zr.STAGING_BULK,) + shape)
+                   sigma=rng.uniform(1e-3, 1e-1, size=len(numels)), staging=(mode,) + shape)
+    assert run.plan.staging == mode
     for s in range(1, 4):
         run.step(s)
         run.check(f"bulk W={W} shape={shape} step {s}: ")
 
 
-def test_bulk_staging_skip_and_scale():
+@pytest.mark.parametrize("mode", [zr.STAGING_BULK, zr.STAGING_BULK_IO])
+def test_bulk_staging_skip_and_scale(mode):
     """A +inf in one bucket skips the whole bulk-staged step and halves the dynamic scale, like the register
     path; switching back to register staging between steps continues the same run."""
     numels = [30_000, 4_000, 70_000]
-    run = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=5,
-                   staging=(zr.STAGING_BULK, 0, 0))
+    run = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=5, staging=(mode, 0, 0))
     rep, orep = run.step(1)
     assert rep.overflow == 0
     before = [x.copy() for x in run.live()]
@@ -521,17 +526,17 @@ def test_bulk_staging_skip_and_scale():
     run.plan.set_staging(zr.STAGING_REGISTERS)
     run.step(3)
     run.check("register staging after bulk: ")
-    run.plan.set_staging(zr.STAGING_BULK)
+    run.plan.set_staging(mode)
     run.step(4)
     run.check("bulk staging again: ")
 
 
-def test_bulk_staging_large_plan_one_block_per_tile():
+@pytest.mark.parametrize("mode", [zr.STAGING_BULK, zr.STAGING_BULK_IO])
+def test_bulk_staging_large_plan_one_block_per_tile(mode):
     """A plan with more than four waves of 32K-element tiles: the bulk-staged step launches one block per
-    tile (the launch shape the benchmark times); sampled against the oracle on a window set."""
+    tile (the launch shape the benchmark times)."""
     w = zrgen.workload("gpt2")
-    run = FusedRun(list(w.tensors)[:25], 8, 1, zr.BF16, cap=w.cap, S=1.0, seed=w.seed,
-                   staging=(zr.STAGING_BULK, 0, 0))
+    run = FusedRun(list(w.tensors)[:25], 8, 1, zr.BF16, cap=w.cap, S=1.0, seed=w.seed, staging=(mode, 0, 0))
     assert run.plan.numel > 4 * 152 * 2 * 32768
     for s in (1, 2):
         run.step(s)
@@ -544,7 +549,7 @@ def test_bulk_staging_rejects_unsupported():
         plan.set_staging(zr.STAGING_BULK)
     plan.close()
     plan = zr.Plan([4096], W=2, A=1, dtype=zr.BF16, stage=2, cap=8192)
-    for bad in ((2, 0, 0), (zr.STAGING_BULK, 12, 0), (zr.STAGING_BULK, 0, 5)):
+    for bad in ((3, 0, 0), (-1, 0, 0), (zr.STAGING_BULK, 12, 0), (zr.STAGING_BULK, 0, 5)):
         with pytest.raises(zr.ZrError):
             plan.set_staging(*bad)
     with pytest.raises(zr.ZrError):  # 4 stages of 65536 elements do not fit an SM

@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libzr.so")
 
 F16, BF16, F32 = 0, 1, 2
-STAGING_REGISTERS, STAGING_BULK = 0, 1  # zr_staging
+STAGING_REGISTERS, STAGING_BULK, STAGING_BULK_IO = 0, 1, 2  # zr_staging
 MAX_W, MAX_REPLICAS, ALIGN = 64, 256, 8
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "out of memory", 5: "timeout"}
 
@@ -577,4 +577,5 @@ def step_noalloc(buckets: np.ndarray, W: int, A: int, dtype: int, grads: Sequenc
 
 __all__ = ["lib", "ZrError", "chunk_size", "bucket_plan", "model_state_bytes", "ring_traffic", "reduce_scatter",
            "all_reduce", "adamw_shard_step", "accumulate", "offload_adamw", "all_gather", "AdamW", "Scaler",
-           "State", "State1", "Plan", "step_noalloc", "F16", "BF16", "F32", "STAGING_REGISTERS", "STAGING_BULK"]
+           "State", "State1", "Plan", "step_noalloc", "F16", "BF16", "F32", "STAGING_REGISTERS", "STAGING_BULK",
+           "STAGING_BULK_IO"]

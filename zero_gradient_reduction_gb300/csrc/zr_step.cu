@@ -76,7 +76,9 @@ static zr_status configure_staging(zr_plan* p, int staging, int stage_elems, int
     p->staging = ZR_STAGING_REGISTERS;
     return ZR_OK;
   }
-  if (staging != ZR_STAGING_BULK) return fail(ZR_ERR_INVALID, "zr_plan_set_staging: unknown staging %d", staging);
+  if (staging != ZR_STAGING_BULK && staging != ZR_STAGING_BULK_IO)
+    return fail(ZR_ERR_INVALID, "zr_plan_set_staging: unknown staging %d", staging);
+  const bool sb = staging == ZR_STAGING_BULK_IO;
   if (p->A != 1 || p->fp32_grads)
     return fail(ZR_ERR_UNSUPPORTED, "zr_plan_set_staging: bulk staging needs A = 1 and 16-bit gradients");
   if (stage_elems < 0 || (stage_elems % 8) != 0 || stage_elems > 65536)
@@ -107,10 +109,14 @@ static zr_status configure_staging(zr_plan* p, int staging, int stage_elems, int
     return fail(ZR_ERR_UNSUPPORTED, "zr_plan_set_staging: %d stages of %d elements need %lld bytes of shared memory "
                 "(a block may have %d)", NS, E, (long long)smem64, optin);
   const int smem = (int)smem64;
-  BulkKernelFn k = p->dtype == ZR_F16 ? pick_bulk_kernel<zr::DT_F16>(p->W) : pick_bulk_kernel<zr::DT_BF16>(p->W);
+  BulkKernelFn k = sb ? (p->dtype == ZR_F16 ? pick_bulk_kernel<zr::DT_F16, true>(p->W)
+                                            : pick_bulk_kernel<zr::DT_BF16, true>(p->W))
+                      : (p->dtype == ZR_F16 ? pick_bulk_kernel<zr::DT_F16, false>(p->W)
+                                            : pick_bulk_kernel<zr::DT_BF16, false>(p->W));
+  const int threads = bulk_threads(sb);
   int per_sm = 0, sms = 0;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kBulkThreads, smem);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
   if (e != cudaSuccess) return cuda_fail("zr_plan_set_staging", e);
   if (per_sm < 1)
@@ -125,7 +131,9 @@ static zr_status configure_staging(zr_plan* p, int staging, int stage_elems, int
   p->bulk_NS = NS;
   p->bulk_smem = smem;
   p->bulk_grid = grid;
-  p->staging = ZR_STAGING_BULK;
+  p->bulk_threads = threads;
+  p->bulk_resident = resident;
+  p->staging = staging;
   return ZR_OK;
 }
 
@@ -266,12 +274,15 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
     zr_plan_destroy(p);
     return ss;
   }
-  // zr_step stages its loads by bulk copies where that applies (A = 1, 16-bit gradients):
-  // measured 1 % faster than register staging on both the 7B (W = 2) and 1.3B (W = 8)
-  // workloads. A plan it does not suit keeps register staging.
-  if (p->A == 1 && !p->fp32_grads && p->ntiles > 0 &&
-      configure_staging(p, ZR_STAGING_BULK, 0, 0) != ZR_OK) {
-    p->staging = ZR_STAGING_REGISTERS;
+  // zr_step stages its loads by bulk copies where that applies (A = 1, 16-bit gradients) and
+  // the plan streams from HBM (at least four waves of tiles): measured 1 % faster than
+  // register staging on both the 7B (W = 2) and 1.3B (W = 8) workloads. A small plan is
+  // launch-bound, and there the ring's fill costs more than it hides (the 786,432-param
+  // workload: 14.5 us against 12.5 us), so it keeps register staging, as do the plans bulk
+  // staging does not cover.
+  if (p->A == 1 && !p->fp32_grads && p->ntiles > 0) {
+    if (configure_staging(p, ZR_STAGING_BULK, 0, 0) != ZR_OK || p->ntiles < 4 * p->bulk_resident)
+      p->staging = ZR_STAGING_REGISTERS;
     zr::clear_error();
   }
   *out = p;
@@ -415,11 +426,11 @@ extern "C" zr_status zr_step(zr_plan* p, int stage, const void* const* grads, co
   zr_status s = check_step_args(p, stage, grads, st, h);
   if (s != ZR_OK) return s;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (p->staging == ZR_STAGING_BULK && p->ntiles > 0) {
+  if (p->staging != ZR_STAGING_REGISTERS && p->ntiles > 0) {
     const FusedArgs a = make_args(p, stage, grads, st->master, st->m, st->v, st->param, h, 0, p->ntiles,
                                   (unsigned)p->bulk_grid);
     const BulkCfg cfg{p->bulk_E, p->bulk_NS};
-    reinterpret_cast<BulkKernelFn>(p->bulk_kernel)<<<p->bulk_grid, kBulkThreads, p->bulk_smem, cs>>>(a, cfg);
+    reinterpret_cast<BulkKernelFn>(p->bulk_kernel)<<<p->bulk_grid, p->bulk_threads, p->bulk_smem, cs>>>(a, cfg);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ZR_ERR_CUDA, "zr_step: launch failed: %s", cudaGetErrorString(e));
   } else {

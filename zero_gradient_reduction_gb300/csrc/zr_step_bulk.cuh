@@ -21,7 +21,10 @@
 namespace {
 
 constexpr int kBulkConsumerWarps = 8;
-constexpr int kBulkThreads = (kBulkConsumerWarps + 1) * 32;
+// threads of a block: the producer warp, the storer warp when stores are bulk too, consumers
+__host__ __device__ constexpr int bulk_threads(bool store_bulk) {
+  return (kBulkConsumerWarps + (store_bulk ? 2 : 1)) * 32;
+}
 constexpr int kBulkMaxStages = 4;
 constexpr uint64_t kBulkWaitNs = 2000000000ull;  // 2 s for one stage is a fault, not a slow step
 
@@ -88,15 +91,39 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
+// `bytes` (a multiple of 16, both addresses 16-byte aligned) from this block's shared memory
+// to global memory, in the executing thread's current bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until the executing thread's bulk groups have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Waits until the executing thread's bulk groups have completed their writes.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Orders this thread's earlier shared-memory writes before later bulk copies that read them.
+__device__ __forceinline__ void fence_to_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Stage layout in shared memory: W replica slices of E 16-bit values (ring position
 // order), then E fp32 master, m and v values.
 __host__ __device__ inline int bulk_stage_bytes(int W, int E) { return W * E * 2 + 12 * E; }
 
-template <int DT, int WT>
-__global__ void __launch_bounds__(kBulkThreads, 2) fused_bulk_kernel(const __grid_constant__ FusedArgs a,
-                                                                     const BulkCfg cfg) {
+// SB (store bulk): the consumers write a stage's results back into its shared-memory slots
+// (the new master/m/v over the old ones, the 16-bit parameter over the first replica slice)
+// and a storer warp (warp 1) copies them out with bulk copies; the stage's slot is released
+// to the producer once those copies have read it. Without SB the consumers store to global
+// memory directly and release the slot themselves.
+template <int DT, int WT, bool SB>
+__global__ void __launch_bounds__(bulk_threads(SB), 2) fused_bulk_kernel(const __grid_constant__ FusedArgs a,
+                                                                         const BulkCfg cfg) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ __align__(8) uint64_t full[kBulkMaxStages], empty[kBulkMaxStages];
+  __shared__ __align__(8) uint64_t full[kBulkMaxStages], empty[kBulkMaxStages], done[kBulkMaxStages];
   __shared__ StageHdr hdr[kBulkMaxStages];
   __shared__ StepConsts s_k;
   __shared__ int s_bad, s_err;
@@ -110,7 +137,8 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fused_bulk_kernel(const __gri
     s_err = 0;
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kBulkConsumerWarps);
+      mbar_init(&empty[s], SB ? 1 : kBulkConsumerWarps);
+      mbar_init(&done[s], kBulkConsumerWarps);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -170,8 +198,32 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fused_bulk_kernel(const __gri
           mbar_wait(&full[(int)(j % NS)], (uint32_t)((j / NS) & 1));
       }
     }
+  } else if (SB && warp == 1) {
+    if (lane == 0) {
+      // storer: once the consumers are done with a stage, copy its results out and release
+      // the slot when the copies have read it
+      for (int64_t it = 0;; ++it) {
+        const int s = (int)(it % NS);
+        if (!mbar_wait(&done[s], (uint32_t)((it / NS) & 1))) {
+          s_err = 1;
+          break;
+        }
+        const StageHdr H = hdr[s];
+        if (H.count == 0) break;
+        unsigned char* base = smem + (size_t)s * stage_bytes;
+        const int64_t e0 = H.start;
+        bulk_store(a.master[out] + e0, base + W * slot16, H.count * 4);
+        bulk_store(a.m[out] + e0, base + W * slot16 + 4 * E, H.count * 4);
+        bulk_store(a.v[out] + e0, base + W * slot16 + 8 * E, H.count * 4);
+        bulk_store(a.param[out] + e0, base, H.count * 2);
+        bulk_commit();
+        bulk_wait_read();
+        mbar_arrive(&empty[s]);
+      }
+      bulk_wait_all();
+    }
   } else {
-    const int ct = threadIdx.x - 32;
+    const int ct = threadIdx.x - (SB ? 64 : 32);
     for (int64_t it = 0;; ++it) {
       const int s = (int)(it % NS);
       if (!mbar_wait(&full[s], (uint32_t)((it / NS) & 1))) {
@@ -179,8 +231,14 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fused_bulk_kernel(const __gri
         break;
       }
       const StageHdr H = hdr[s];
-      if (H.count == 0) break;
-      const unsigned char* base = smem + (size_t)s * stage_bytes;
+      if (H.count == 0) {
+        if (SB) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&done[s]);  // tells the storer the block's work is over
+        }
+        break;
+      }
+      unsigned char* base = smem + (size_t)s * stage_bytes;
       const int groups = H.count / 8;
       for (int g = ct; g < groups; g += kBulkConsumerWarps * 32) {
         float sum[8];
@@ -201,13 +259,39 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fused_bulk_kernel(const __gri
             for (int j = 0; j < 8; ++j) sum[j] = __fadd_rn(sum[j], x[j]);
           }
         }
-        const float4* ps = reinterpret_cast<const float4*>(base + W * slot16) + 2 * g;
-        const float4* ms = reinterpret_cast<const float4*>(base + W * slot16 + 4 * E) + 2 * g;
-        const float4* vs = reinterpret_cast<const float4*>(base + W * slot16 + 8 * E) + 2 * g;
-        bad |= update_group<DT>(a, K, out, H.start + (int64_t)g * 8, sum, ps[0], ps[1], ms[0], ms[1], vs[0], vs[1]);
+        float4* ps = reinterpret_cast<float4*>(base + W * slot16) + 2 * g;
+        float4* ms = reinterpret_cast<float4*>(base + W * slot16 + 4 * E) + 2 * g;
+        float4* vs = reinterpret_cast<float4*>(base + W * slot16 + 8 * E) + 2 * g;
+        if constexpr (SB) {
+          const float4 p0 = ps[0], p1 = ps[1], m0 = ms[0], m1 = ms[1], v0 = vs[0], v1 = vs[1];
+          float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+          float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+          float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            bad |= zr::nonfinite(sum[j]);
+            zr::adamw_elem(__fmul_rn(sum[j], K.r), p[j], m[j], v[j], K.k);
+          }
+          ps[0] = make_float4(p[0], p[1], p[2], p[3]);
+          ps[1] = make_float4(p[4], p[5], p[6], p[7]);
+          ms[0] = make_float4(m[0], m[1], m[2], m[3]);
+          ms[1] = make_float4(m[4], m[5], m[6], m[7]);
+          vs[0] = make_float4(v[0], v[1], v[2], v[3]);
+          vs[1] = make_float4(v[4], v[5], v[6], v[7]);
+          *reinterpret_cast<uint4*>(base + g * 16) = zr::pack8<DT>(p);  // over this group's first replica values
+        } else {
+          bad |= update_group<DT>(a, K, out, H.start + (int64_t)g * 8, sum, ps[0], ps[1], ms[0], ms[1], vs[0],
+                                  vs[1]);
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if constexpr (SB) {
+        fence_to_async();  // the results written above, before the storer's bulk copies read them
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&done[s]);
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
     }
   }
 
@@ -232,12 +316,12 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fused_bulk_kernel(const __gri
 
 using BulkKernelFn = void (*)(FusedArgs, BulkCfg);
 
-template <int DT>
+template <int DT, bool SB>
 BulkKernelFn pick_bulk_kernel(int W) {
   switch (W) {
-    case 2: return fused_bulk_kernel<DT, 2>;
-    case 8: return fused_bulk_kernel<DT, 8>;
-    default: return fused_bulk_kernel<DT, 0>;
+    case 2: return fused_bulk_kernel<DT, 2, SB>;
+    case 8: return fused_bulk_kernel<DT, 8, SB>;
+    default: return fused_bulk_kernel<DT, 0, SB>;
   }
 }
 
