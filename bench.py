@@ -425,9 +425,10 @@ def _measure_step(args, w, zr, plan, hyper, state, grads, dev, stream, ws, gpu_i
         traffic, _digest = _traffic_record(w.name, "inplace_step", "traffic_bytes_per_step")
         kernel = ("fused_step_kernel flag pass + in-place update (bytes and time of the step's two launches "
                   "together)")
-    elif staging == "bulk":
-        traffic, _digest = _traffic_record(w.name, "fused_bulk", files=KERNEL_FILES["bulk"])
-        kernel = "fused_bulk_kernel (one launch per step; loads staged by cp.async.bulk into shared memory)"
+    elif staging in ("bulk", "bulk_io"):
+        traffic, _digest = _traffic_record(w.name, TRAFFIC_PREFIX[staging], files=KERNEL_FILES[staging])
+        kernel = ("fused_bulk_kernel (one launch per step; loads staged by cp.async.bulk into shared memory" +
+                  (", results written back by cp.async.bulk)" if staging == "bulk_io" else ")"))
     else:
         traffic, _digest = _traffic_record(w.name)
         kernel = "fused_step_kernel (one launch per step; loads staged in registers)"
@@ -443,11 +444,13 @@ def _measure_step(args, w, zr, plan, hyper, state, grads, dev, stream, ws, gpu_i
 
 # the fused kernels' source files, whose hash a committed traffic record must match
 KERNEL_FILES = {"registers": ("zr_step_kernel.cuh", "zr_device.cuh"),
-                "bulk": ("zr_step_bulk.cuh", "zr_step_kernel.cuh", "zr_device.cuh")}
+                "bulk": ("zr_step_bulk.cuh", "zr_step_kernel.cuh", "zr_device.cuh"),
+                "bulk_io": ("zr_step_bulk.cuh", "zr_step_kernel.cuh", "zr_device.cuh")}
+TRAFFIC_PREFIX = {"registers": "fused_step", "bulk": "fused_bulk", "bulk_io": "fused_bulk_io"}
 
 
 def _staging_name(zr, plan) -> str:
-    return "bulk" if plan.staging == zr.STAGING_BULK else "registers"
+    return {zr.STAGING_BULK: "bulk", zr.STAGING_BULK_IO: "bulk_io"}.get(plan.staging, "registers")
 
 
 def _measure_other_staging(args, w, zr, plan, hyper, state, grads, dev, stream, steps=20):
@@ -483,7 +486,7 @@ def _measure_other_staging(args, w, zr, plan, hyper, state, grads, dev, stream, 
     ms = e0.elapsed_time(e1) / steps
     peak, _ = _peaks()
     achieved = rep.bytes_alg / (ms * 1e-3) / 1e9
-    traffic, _ = _traffic_record(w.name, "fused_bulk" if name == "bulk" else "fused_step", files=KERNEL_FILES[name])
+    traffic, _ = _traffic_record(w.name, TRAFFIC_PREFIX[name], files=KERNEL_FILES[name])
     return {"staging": name, "ms_per_step": ms, "Gparams_per_s": plan.n_real / ms / 1e6, "hbm_GBs": achieved,
             "frac_of_measured_copy": achieved / peak, "traffic": traffic, "steps": steps,
             "call": "zr_step after zr_plan_set_staging to the other staging, captured as a CUDA graph"}
@@ -551,7 +554,8 @@ def run_zr(args, w):
     inplace_main = args.inplace or w.state_sets == 1
     plan, hyper, state, grads = _setup(w, zr, zrgen, dev, stream, inplace_main)
     if args.staging:
-        plan.set_staging(zr.STAGING_BULK if args.staging == "bulk" else zr.STAGING_REGISTERS)
+        plan.set_staging({"bulk": zr.STAGING_BULK, "bulk_io": zr.STAGING_BULK_IO,
+                          "registers": zr.STAGING_REGISTERS}[args.staging])
     n = plan.numel
     main = _measure_step(args, w, zr, plan, hyper, state, grads, dev, stream, ws, gpu_index, inplace_main)
     ms_step, value, step_bytes = main["ms_step"], main["value"], main["step_bytes"]
@@ -874,7 +878,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chain", action="store_true")
     ap.add_argument("--chain-steps", type=int, default=5)
-    ap.add_argument("--staging", choices=["bulk", "registers"], default=None,
+    ap.add_argument("--staging", choices=["bulk", "bulk_io", "registers"], default=None,
                     help="load staging of the main step's zr_step (default: the plan's own choice)")
     ap.add_argument("--inplace", action="store_true",
                     help="time zr_step_inplace on one state set as the main step (always so for 13b)")
