@@ -310,6 +310,15 @@ zr_status zr_plan_set_staging(zr_plan* p, int staging, int stage_elems, int stag
 /* The staging zr_step uses for plan p (a zr_staging value); -1 for a null plan. */
 int zr_plan_staging(const zr_plan* p);
 
+/* Test hook for the bounded waits of bulk staging; never needed in use. While on != 0,
+ * every stage of a bulk-staged zr_step announces 16 bytes more on its mbarrier than its
+ * copies deliver, so no stage completes: every wait runs out after its 2 s limit (no fault,
+ * no trap, no endless wait; the copies themselves land), the step is skipped with the state
+ * unchanged and zr_plan_report returns ZR_ERR_TIMEOUT until zr_plan_reset. Lets a test check
+ * that a timed-out step reports its error and leaves the CUDA context usable. Errors:
+ * ZR_ERR_INVALID for a null plan. */
+zr_status zr_plan_stall_bulk_waits(zr_plan* p, int on);
+
 /* The optimizer state and the parameter replica as ONE set (zr_step_inplace). Device
  * pointers, zr_plan_numel elements each; param is of the plan's dtype. */
 typedef struct {

@@ -543,6 +543,39 @@ def test_bulk_staging_large_plan_one_block_per_tile(mode):
         run.check(f"large bulk step {s}: ")
 
 
+@pytest.mark.parametrize("mode", [zr.STAGING_BULK, zr.STAGING_BULK_IO])
+def test_bulk_wait_timeout_reports_and_recovers(mode):
+    """The bounded waits of bulk staging: with the test hook on, no stage's copies complete its barrier, so every
+    wait runs out after its limit (2 s), the step is skipped with the live set unchanged, zr_plan_report returns
+    ZR_ERR_TIMEOUT and the CUDA context stays usable; restoring the step state clears the error and the run
+    continues, bit-exact against the oracle."""
+    import time
+    run = FusedRun([40_000, 3_000], 2, 1, zr.F16, cap=50_000, S=1024.0, seed=31, staging=(mode, 0, 0))
+    run.step(1)
+    run.check("before the stalled step: ")
+    ck = run.plan.checkpoint()
+    before = [x.copy() for x in run.live()]
+    cs = torch.cuda.current_stream().cuda_stream
+    for r in range(2):
+        run.layout.grads_dev(run.grads[r], 2, r, run.S, run.table, cs)
+    assert zr.lib().zr_plan_stall_bulk_waits(run.plan._h, 1) == 0
+    t0 = time.perf_counter()
+    run.plan.step(run.grads, run.state, HYPER)  # no report: the call itself does not wait
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert zr.lib().zr_plan_stall_bulk_waits(run.plan._h, 0) == 0
+    assert 1.5 < elapsed < 60.0, elapsed
+    with pytest.raises(zr.ZrError) as err:
+        run.plan.report()
+    assert err.value.status == 5 and "gave up" in str(err.value)
+    assert all(np.array_equal(a, b) for a, b in zip(before, run.live()))
+    x = torch.arange(1024, device="cuda", dtype=torch.float32)  # the context still works
+    assert float(x.sum()) == 1024 * 1023 / 2
+    run.plan.restore(ck)  # a fresh control block with the step state before the stalled step
+    run.step(2)
+    run.check("after recovery: ")
+
+
 def test_bulk_staging_rejects_unsupported():
     plan = zr.Plan([4096], W=2, A=4, dtype=zr.BF16, stage=2, cap=8192)
     with pytest.raises(zr.ZrError):

@@ -102,6 +102,7 @@ def lib():
                 "zr_plan_set_bucket_blocks": (st, [vp, i32]),
                 "zr_plan_set_staging": (st, [vp, i32, i32, i32]),
                 "zr_plan_staging": (i32, [vp]),
+                "zr_plan_stall_bulk_waits": (st, [vp, i32]),
                 "zr_offload_adamw": (st, [vp, vp, vp, vp, vp, i32, i64, ctypes.POINTER(Hyper), ctypes.c_float, i32,
                                           i64, i32, ctypes.POINTER(ctypes.c_int32)]),
                 "zr_offload_step": (st, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(Hyper),

@@ -29,6 +29,7 @@ struct zr_plan {
   void* bulk_kernel = nullptr;
   int bulk_E = 0, bulk_NS = 0, bulk_smem = 0, bulk_grid = 0, bulk_threads = 0;
   int64_t bulk_resident = 0;  // blocks of the bulk kernel that fit on the GPU at once
+  int bulk_stall = 0;         // test hook (zr_plan_stall_bulk_waits): stages announce bytes never sent
   int device = 0;
   // bucketed launches (zr_step_bucket): bucket b's tiles are [tile_begin[b], tile_begin[b+1]),
   // launched with bucket_grid[b] blocks; a step's launches add up to bucket_blocks blocks

@@ -145,6 +145,13 @@ extern "C" zr_status zr_plan_set_staging(zr_plan* p, int staging, int stage_elem
 
 extern "C" int zr_plan_staging(const zr_plan* p) { return p ? p->staging : -1; }
 
+extern "C" zr_status zr_plan_stall_bulk_waits(zr_plan* p, int on) {
+  zr::clear_error();
+  if (!p) return fail(ZR_ERR_INVALID, "zr_plan_stall_bulk_waits: null plan");
+  p->bulk_stall = on ? 1 : 0;
+  return ZR_OK;
+}
+
 extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   zr::clear_error();
   if (!d || !out) return fail(ZR_ERR_INVALID, "zr_plan_create: null argument");
@@ -429,7 +436,7 @@ extern "C" zr_status zr_step(zr_plan* p, int stage, const void* const* grads, co
   if (p->staging != ZR_STAGING_REGISTERS && p->ntiles > 0) {
     const FusedArgs a = make_args(p, stage, grads, st->master, st->m, st->v, st->param, h, 0, p->ntiles,
                                   (unsigned)p->bulk_grid);
-    const BulkCfg cfg{p->bulk_E, p->bulk_NS};
+    const BulkCfg cfg{p->bulk_E, p->bulk_NS, p->bulk_stall ? 16u : 0u};
     reinterpret_cast<BulkKernelFn>(p->bulk_kernel)<<<p->bulk_grid, p->bulk_threads, p->bulk_smem, cs>>>(a, cfg);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ZR_ERR_CUDA, "zr_step: launch failed: %s", cudaGetErrorString(e));

@@ -29,8 +29,9 @@ constexpr int kBulkMaxStages = 4;
 constexpr uint64_t kBulkWaitNs = 2000000000ull;  // 2 s for one stage is a fault, not a slow step
 
 struct BulkCfg {
-  int E;   // elements per stage (a multiple of 8)
-  int NS;  // stages in the ring (<= kBulkMaxStages)
+  int E;             // elements per stage (a multiple of 8)
+  int NS;            // stages in the ring (<= kBulkMaxStages)
+  uint32_t stall_tx; // test hook: bytes announced on every stage beyond those copied (0 in use)
 };
 
 struct StageHdr {
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(bulk_threads(SB), 2) fused_bulk_kernel(const _
           hdr[s].start = e0;
           hdr[s].count = cnt;
           hdr[s].c = c;
-          mbar_arrive_tx(&full[s], (uint32_t)bulk_stage_bytes(W, cnt));
+          mbar_arrive_tx(&full[s], (uint32_t)bulk_stage_bytes(W, cnt) + cfg.stall_tx);
           unsigned char* base = smem + (size_t)s * stage_bytes;
           for (int h = 0; h < W; ++h) {
             int pos = c + h;  // c < W and h < W
