@@ -1,8 +1,11 @@
-/* One fused step driven from plain C through zr.h: cudaMalloc'd buffers, no Python and
+/* Three fused steps driven from plain C through zr.h: cudaMalloc'd buffers, no Python and
  * no torch. Every gradient is 1.0 on W = 4 workers with loss scale 1, so the mean
- * gradient is 1 and the first AdamW step (m = 0.1, v = 0.001, bias corrections 0.1 and
- * 0.001, no weight decay) moves every master value from 0.5 to 0.5 - lr / (1 + eps).
- * Prints "ok" and returns 0 on success. */
+ * gradient is 1 at every step; with a constant gradient, bias-corrected m and v are both
+ * 1 at every step t (m = 1 - 0.9^t and v = 1 - 0.999^t before correction), so each step
+ * (no weight decay) moves every master value by -lr / (1 + eps): 0.5 - t * lr / (1 + eps)
+ * after step t. Step 1 runs zr_step as the plan chose, step 2 zr_step with bulk-copy
+ * staging, step 3 zr_step_noalloc on the plan's bucket table. Prints "ok" and returns 0
+ * on success. */
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -16,6 +19,20 @@
 static int fail_cuda(const char* what, cudaError_t e) {
     printf("%s: %s\n", what, cudaGetErrorString(e));
     return 1;
+}
+
+/* every master value after step t: 0.5 - t * lr / (1 + eps), lr = 1e-3, eps = 1e-8 */
+static int check_master(const float* dev, float* host, int64_t n, int t) {
+    cudaError_t e = cudaMemcpy(host, dev, (size_t)n * 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda("read back", e);
+    const double want = 0.5 - t * 1e-3 / (1.0 + 1e-8);
+    for (int64_t i = 0; i < n; ++i) {
+        if (fabs((double)host[i] - want) > 2e-6) {
+            printf("step %d: master[%lld] = %.9g, want %.9g\n", t, (long long)i, host[i], want);
+            return 1;
+        }
+    }
+    return 0;
 }
 
 int main(void) {
@@ -81,15 +98,42 @@ int main(void) {
                (long long)rep.n_real);
         return 1;
     }
-    e = cudaMemcpy(f32, st.master[1], (size_t)n * 4, cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return fail_cuda("read back", e);
-    const double want = 0.5 - 1e-3 / (1.0 + 1e-8);
-    for (int64_t i = 0; i < n; ++i) {
-        if (fabs((double)f32[i] - want) > 1e-6) {
-            printf("master[%lld] = %.9g, want %.9g\n", (long long)i, f32[i], want);
-            return 1;
-        }
+    if (check_master(st.master[1], f32, n, 1) != 0) return 1;
+
+    /* step 2: loads staged through shared memory by bulk copies */
+    if (zr_plan_set_staging(p, ZR_STAGING_BULK, 0, 0) != ZR_OK || zr_plan_staging(p) != ZR_STAGING_BULK) {
+        printf("zr_plan_set_staging: %s\n", zr_last_error());
+        return 1;
     }
+    if (zr_step(p, 2, (const void* const*)grads, &st, &h, NULL, &rep) != ZR_OK || rep.t != 2 || rep.current != 0) {
+        printf("zr_step (bulk): %s t=%lld current=%d\n", zr_last_error(), (long long)rep.t, rep.current);
+        return 1;
+    }
+    if (check_master(st.master[0], f32, n, 2) != 0) return 1;
+
+    /* step 3: the no-allocation entry point on the plan's bucket table; the caller carries the
+     * live set (0), the loss scale (1) and t (3) */
+    const int nb = zr_plan_nbuckets(p);
+    zr_bucket* buckets = (zr_bucket*)malloc((size_t)nb * sizeof(zr_bucket));
+    int32_t* overflow = NULL;
+    if (!buckets || zr_plan_buckets(p, buckets, NULL) != ZR_OK) return 1;
+    e = cudaMalloc((void**)&overflow, sizeof(int32_t));
+    if (e != cudaSuccess) return fail_cuda("overflow", e);
+    if (zr_step_noalloc(buckets, nb, NWORKERS, 1, ZR_BF16, NULL, (const void* const*)grads, &st, 0, &h, 1.0f, 3,
+                        overflow, NULL) != ZR_OK) {
+        printf("zr_step_noalloc: %s\n", zr_last_error());
+        return 1;
+    }
+    int32_t flag = -1;
+    e = cudaMemcpy(&flag, overflow, sizeof flag, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda("overflow read back", e);
+    if (flag != 0) {
+        printf("zr_step_noalloc: overflow %d\n", flag);
+        return 1;
+    }
+    if (check_master(st.master[1], f32, n, 3) != 0) return 1;
+    cudaFree(overflow);
+    free(buckets);
     zr_plan_destroy(p);
     for (int w = 0; w < NWORKERS; ++w) cudaFree(grads[w]);
     for (int k = 0; k < 2; ++k) {

@@ -1,5 +1,6 @@
 """The C ABI used from plain C: tests/c_abi_step.c includes only zr.h and the CUDA runtime, allocates with
-cudaMalloc and runs one fused step through libzr.so, checking the result against its closed form."""
+cudaMalloc and runs three fused steps through libzr.so (the plan's staging, bulk-copy staging, and
+zr_step_noalloc), checking each result against its closed form."""
 import os
 import subprocess
 
