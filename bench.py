@@ -795,7 +795,10 @@ def run_zr(args, w):
 
     rep_buckets = plan.buckets
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        params, secs, what = oracle_sample(w, plan.buckets, plan.tensor_offsets, args.cpu_seconds)
+        import oracle
+        oracle.build()
+        ob, ooffs = oracle.bucket_plan(list(w.tensors), w.cap, w.W)  # the oracle's own table, not the plan's
+        params, secs, what = oracle_sample(w, ob, ooffs, args.cpu_seconds)
         cpu = {"value": params / secs / 1e9, "unit": "Gparams/s", "cores": 1, "kind": "oracle",
                "sample": f"{what}, step 1 inputs; {secs:.1f} s single-threaded on the host"}
 
