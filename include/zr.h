@@ -287,7 +287,8 @@ zr_status zr_step_bucket(zr_plan* p, int stage, int bucket, const void* const* g
  * blocks of all its launches). Errors: ZR_ERR_INVALID for a null plan or max_blocks < 0. */
 zr_status zr_plan_set_bucket_blocks(zr_plan* p, int max_blocks);
 
-/* How zr_step moves a tile's inputs into the SMs. ZR_STAGING_REGISTERS: every thread
+/* How zr_step moves a tile's inputs into the SMs (a launch setting; the pages have no
+ * counterpart: their step runs in NCCL and the optimizer). ZR_STAGING_REGISTERS: every thread
  * issues its 16-byte loads of the W replicas and of master/m/v into registers before any
  * arithmetic. ZR_STAGING_BULK: a producer warp per block copies each stage of a tile
  * (stage_elems elements of the W replicas and of master/m/v) into shared memory with
@@ -296,13 +297,15 @@ zr_status zr_plan_set_bucket_blocks(zr_plan* p, int max_blocks);
  * Both give the same bytes; only speed differs. Bulk staging covers zr_step (and its CUDA
  * graph capture) for plans with A = 1 and 16-bit gradients, and is what zr_plan_create
  * chooses for such a plan when it has at least four waves of tiles (a plan that streams
- * from HBM; automatic shape); other plans, and the other calls, use register staging. stage_elems = 0 and stages = 0 choose a shape that lets two blocks share an SM.
+ * from HBM; automatic shape); other plans, and the other calls, use register staging.
+ * stage_elems = 0 and stages = 0 choose a shape that lets two blocks share an SM. Call it
+ * between steps; a CUDA graph captured earlier keeps the kernel it captured.
  * Every wait of a bulk-staged step is bounded (2 s); one that gives up skips the step and
  * makes zr_plan_report (and zr_step with a report) return ZR_ERR_TIMEOUT until
  * zr_plan_reset. Errors: ZR_ERR_INVALID (null plan, unknown staging, stage_elems not 0 or a
  * multiple of 8 up to 65536, stages above 4), ZR_ERR_UNSUPPORTED (A > 1, fp32 gradients, a
- * shape that does not fit an SM's shared memory), ZR_ERR_CUDA. */
-/* ZR_STAGING_BULK_IO: as ZR_STAGING_BULK, and the results go out the same way: the consumers
+ * shape that does not fit an SM's shared memory), ZR_ERR_CUDA.
+ * ZR_STAGING_BULK_IO: as ZR_STAGING_BULK, and the results go out the same way: the consumers
  * write each stage's new master/m/v and 16-bit parameter back into its shared-memory slots
  * and a storer warp copies them to state set 1-k with bulk copies (shared to global). */
 typedef enum { ZR_STAGING_REGISTERS = 0, ZR_STAGING_BULK = 1, ZR_STAGING_BULK_IO = 2 } zr_staging;
