@@ -44,10 +44,9 @@ def test_random_plan_matches_oracle(case):
     dynamic = bool(rng.integers(0, 2))
     sigma = rng.uniform(1e-3, 1e-1, size=ntensors)
     cls = InPlaceRun if rng.integers(0, 2) else FusedRun
-    # the plan's own staging, or one chosen (bulk staging applies to A = 1 only)
+    # the plan's own staging, or one chosen
     pick = int(rng.integers(0, 4))
-    staging = None if pick == 0 or (A > 1 and pick > 1) else \
-        ((zr.STAGING_REGISTERS, zr.STAGING_BULK, zr.STAGING_BULK_IO)[pick - 1], 0, 0)
+    staging = None if pick == 0 else ((zr.STAGING_REGISTERS, zr.STAGING_BULK, zr.STAGING_BULK_IO)[pick - 1], 0, 0)
     run = cls(numels, W, A, dtype, cap=cap, S=S, dynamic=dynamic, order=order, seed=case, sigma=sigma,
               interval=2, staging=staging)
     where = f"case {case}: W={W} A={A} dtype={dtype} cap={cap} numels={numels} {cls.__name__}"

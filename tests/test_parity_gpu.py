@@ -331,8 +331,6 @@ def test_fused_tiny_config_bit_exact(staging):
                                        (17, 1, zr.BF16), (24, 1, zr.F16), (33, 1, zr.BF16)])
 @pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
 def test_fused_ragged_buckets(W, A, dtype, staging):
-    if A > 1 and staging is not None:
-        pytest.skip("bulk staging covers A = 1 only")
     rng = np.random.default_rng(W * 100 + A)
     numels = [1000, 37, 5000, 8, 123_457, 64, 9_999, 3, 40_000]
     order = list(rng.permutation(W))
@@ -491,23 +489,28 @@ def test_checkpoint_resume_is_byte_identical():
 
 
 # ----------------------------------------------------------------------------- bulk-copy staging
-@pytest.mark.parametrize("W,dtype,shape", [(1, zr.BF16, (0, 0)), (2, zr.F16, (0, 0)), (2, zr.BF16, (256, 2)),
-                                           (3, zr.F16, (0, 0)), (5, zr.BF16, (1024, 4)), (8, zr.BF16, (0, 0)),
-                                           (8, zr.F16, (4096, 1)), (16, zr.F16, (0, 0)), (64, zr.BF16, (0, 0))])
+@pytest.mark.parametrize("W,A,dtype,shape", [(1, 1, zr.BF16, (0, 0)), (2, 1, zr.F16, (0, 0)),
+                                             (2, 1, zr.BF16, (256, 2)), (3, 1, zr.F16, (0, 0)),
+                                             (5, 1, zr.BF16, (1024, 4)), (8, 1, zr.BF16, (0, 0)),
+                                             (8, 1, zr.F16, (4096, 1)), (16, 1, zr.F16, (0, 0)),
+                                             (64, 1, zr.BF16, (0, 0)), (2, 4, zr.BF16, (0, 0)), (4, 4, zr.F16, (0, 0)),
+                                             (8, 4, zr.BF16, (0, 0)), (3, 3, zr.BF16, (512, 3)),
+                                             (32, 8, zr.F16, (0, 0))])
 @pytest.mark.parametrize("mode", [zr.STAGING_BULK, zr.STAGING_BULK_IO])
-def test_bulk_staging_bit_exact(W, dtype, shape, mode):
+def test_bulk_staging_bit_exact(W, A, dtype, shape, mode):
     """zr_step with its loads (and with BULK_IO its results too) staged in shared memory by bulk copies gives
-    the oracle's bytes: ragged buckets, a ring order, automatic and explicit stage shapes (down to stages of
-    256 elements and a single stage)."""
-    rng = np.random.default_rng(W * 31 + dtype)
+    the oracle's bytes: ragged buckets, a ring order, micro-batch accumulation (A > 1, up to W*A = 256 replica
+    slices per stage), automatic and explicit stage shapes (down to stages of 256 elements and a single
+    stage)."""
+    rng = np.random.default_rng(W * 31 + A * 7 + dtype)
     numels = [1000, 37, 5000, 8, 123_457, 64, 9_999, 3, 40_000]
     order = [int(x) for x in rng.permutation(W)]
-    run = FusedRun(numels, W, 1, dtype, cap=20_000, S=8.0, order=order, seed=21,
+    run = FusedRun(numels, W, A, dtype, cap=20_000, S=8.0, order=order, seed=21,
                    sigma=rng.uniform(1e-3, 1e-1, size=len(numels)), staging=(mode,) + shape)
     assert run.plan.staging == mode
     for s in range(1, 4):
         run.step(s)
-        run.check(f"bulk W={W} shape={shape} step {s}: ")
+        run.check(f"bulk W={W} A={A} shape={shape} step {s}: ")
 
 
 @pytest.mark.parametrize("mode", [zr.STAGING_BULK, zr.STAGING_BULK_IO])
@@ -577,8 +580,8 @@ def test_bulk_wait_timeout_reports_and_recovers(mode):
 
 
 def test_bulk_staging_rejects_unsupported():
-    plan = zr.Plan([4096], W=2, A=4, dtype=zr.BF16, stage=2, cap=8192)
-    with pytest.raises(zr.ZrError):
+    plan = zr.Plan([4096], W=2, A=1, dtype=zr.BF16, stage=2, cap=8192, fp32_grads=True)
+    with pytest.raises(zr.ZrError):  # bulk staging needs 16-bit gradients
         plan.set_staging(zr.STAGING_BULK)
     plan.close()
     plan = zr.Plan([4096], W=2, A=1, dtype=zr.BF16, stage=2, cap=8192)

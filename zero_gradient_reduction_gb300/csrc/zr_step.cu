@@ -79,8 +79,8 @@ static zr_status configure_staging(zr_plan* p, int staging, int stage_elems, int
   if (staging != ZR_STAGING_BULK && staging != ZR_STAGING_BULK_IO)
     return fail(ZR_ERR_INVALID, "zr_plan_set_staging: unknown staging %d", staging);
   const bool sb = staging == ZR_STAGING_BULK_IO;
-  if (p->A != 1 || p->fp32_grads)
-    return fail(ZR_ERR_UNSUPPORTED, "zr_plan_set_staging: bulk staging needs A = 1 and 16-bit gradients");
+  if (p->fp32_grads) return fail(ZR_ERR_UNSUPPORTED, "zr_plan_set_staging: bulk staging needs 16-bit gradients");
+  const int R = p->W * p->A;  // replica slices per stage
   if (stage_elems < 0 || (stage_elems % 8) != 0 || stage_elems > 65536)
     return fail(ZR_ERR_INVALID, "zr_plan_set_staging: stage_elems must be 0 or a multiple of 8 up to 65536");
   if (stages < 0 || stages > kBulkMaxStages)
@@ -95,13 +95,13 @@ static zr_status configure_staging(zr_plan* p, int staging, int stage_elems, int
   int E = stage_elems, NS = stages;
   if (E == 0) {
     E = 2048;
-    while (E > 256 && 2 * bulk_stage_bytes(p->W, E) > kBulkBudget) E /= 2;
+    while (E > 256 && 2 * bulk_stage_bytes(R, E) > kBulkBudget) E /= 2;
   }
-  if (NS == 0) {
-    NS = kBulkBudget / bulk_stage_bytes(p->W, E);
-    NS = NS < 2 ? 2 : NS > kBulkMaxStages ? kBulkMaxStages : NS;
+  if (NS == 0) {  // a stage larger than the budget (hundreds of replica slices) runs alone on its SM
+    NS = kBulkBudget / bulk_stage_bytes(R, E);
+    NS = NS < 1 ? 1 : NS > kBulkMaxStages ? kBulkMaxStages : NS;
   }
-  const int64_t smem64 = (int64_t)NS * bulk_stage_bytes(p->W, E);
+  const int64_t smem64 = (int64_t)NS * bulk_stage_bytes(R, E);
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
   if (e != cudaSuccess) return cuda_fail("zr_plan_set_staging", e);
@@ -109,10 +109,10 @@ static zr_status configure_staging(zr_plan* p, int staging, int stage_elems, int
     return fail(ZR_ERR_UNSUPPORTED, "zr_plan_set_staging: %d stages of %d elements need %lld bytes of shared memory "
                 "(a block may have %d)", NS, E, (long long)smem64, optin);
   const int smem = (int)smem64;
-  BulkKernelFn k = sb ? (p->dtype == ZR_F16 ? pick_bulk_kernel<zr::DT_F16, true>(p->W)
-                                            : pick_bulk_kernel<zr::DT_BF16, true>(p->W))
-                      : (p->dtype == ZR_F16 ? pick_bulk_kernel<zr::DT_F16, false>(p->W)
-                                            : pick_bulk_kernel<zr::DT_BF16, false>(p->W));
+  BulkKernelFn k = sb ? (p->dtype == ZR_F16 ? pick_bulk_kernel<zr::DT_F16, true>(p->W, p->A)
+                                            : pick_bulk_kernel<zr::DT_BF16, true>(p->W, p->A))
+                      : (p->dtype == ZR_F16 ? pick_bulk_kernel<zr::DT_F16, false>(p->W, p->A)
+                                            : pick_bulk_kernel<zr::DT_BF16, false>(p->W, p->A));
   const int threads = bulk_threads(sb);
   int per_sm = 0, sms = 0;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -4,15 +4,18 @@
 // of each stage of a tile reach shared memory through one-dimensional cp.async.bulk copies
 // (this GPU's own memory, no multicast, no cluster), so no register holds a load in flight.
 //
-// A block is one producer warp and kBulkConsumerWarps consumer warps. The producer walks
-// the block's tiles in stages of E elements and keeps a ring of NS stages filled: it
-// waits until the consumers have released a stage (the stage's `empty` barrier), announces
-// the stage's bytes on its `full` barrier and issues W + 3 bulk copies that complete on it.
-// The consumers wait for a stage's `full` barrier, fold the W replicas in ring order,
-// update the 8-element groups and store the results straight to global memory, then
-// release the stage. No block barrier is taken inside the loop. Every wait gives up after
-// kBulkWaitNs and records an error in the control block; the step is then skipped and
-// zr_plan_report returns ZR_ERR_TIMEOUT.
+// A block is one producer warp and kBulkConsumerWarps consumer warps (plus a storer warp
+// when the results leave by bulk copies too). The producer walks the block's tiles in
+// stages of E elements and keeps a ring of NS stages filled: it waits until a stage has
+// been released (the stage's `empty` barrier), announces the stage's bytes on its `full`
+// barrier and issues W + 3 bulk copies that complete on it. The consumers wait for a
+// stage's `full` barrier, fold the W replicas in ring order, update the 8-element groups
+// and store the results straight to global memory, then release the stage; or, with the
+// storer, write the results back into the stage's slots and signal the storer (`done`),
+// which copies them out and releases the stage once its copies have read it. No block
+// barrier is taken inside the loop. Every wait gives up after kBulkWaitNs and records an
+// error in the control block; the step is then skipped and zr_plan_report returns
+// ZR_ERR_TIMEOUT.
 #pragma once
 #include <cuda_runtime.h>
 
@@ -111,16 +114,16 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // Orders this thread's earlier shared-memory writes before later bulk copies that read them.
 __device__ __forceinline__ void fence_to_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// Stage layout in shared memory: W replica slices of E 16-bit values (ring position
-// order), then E fp32 master, m and v values.
-__host__ __device__ inline int bulk_stage_bytes(int W, int E) { return W * E * 2 + 12 * E; }
+// Stage layout in shared memory: R = W*A replica slices of E 16-bit values (ring position
+// order, each worker's A micro-batches together), then E fp32 master, m and v values.
+__host__ __device__ inline int bulk_stage_bytes(int R, int E) { return R * E * 2 + 12 * E; }
 
 // SB (store bulk): the consumers write a stage's results back into its shared-memory slots
 // (the new master/m/v over the old ones, the 16-bit parameter over the first replica slice)
 // and a storer warp (warp 1) copies them out with bulk copies; the stage's slot is released
 // to the producer once those copies have read it. Without SB the consumers store to global
 // memory directly and release the slot themselves.
-template <int DT, int WT, bool SB>
+template <int DT, int WT, int AT, bool SB>
 __global__ void __launch_bounds__(bulk_threads(SB), 2) fused_bulk_kernel(const __grid_constant__ FusedArgs a,
                                                                          const BulkCfg cfg) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -130,8 +133,10 @@ __global__ void __launch_bounds__(bulk_threads(SB), 2) fused_bulk_kernel(const _
   __shared__ int s_bad, s_err;
   __shared__ unsigned s_ticket;
   const int W = WT > 0 ? WT : a.W;
+  const int A = AT > 0 ? AT : a.A;
+  const int R = W * A;  // replica slices per stage
   const int E = cfg.E, NS = cfg.NS;
-  const int slot16 = E * 2, stage_bytes = bulk_stage_bytes(W, E);
+  const int slot16 = E * 2, stage_bytes = bulk_stage_bytes(R, E);
   if (threadIdx.x == 0) {
     read_consts(a, s_k);
     s_bad = 0;
@@ -168,17 +173,18 @@ __global__ void __launch_bounds__(bulk_threads(SB), 2) fused_bulk_kernel(const _
           hdr[s].start = e0;
           hdr[s].count = cnt;
           hdr[s].c = c;
-          mbar_arrive_tx(&full[s], (uint32_t)bulk_stage_bytes(W, cnt) + cfg.stall_tx);
+          mbar_arrive_tx(&full[s], (uint32_t)bulk_stage_bytes(R, cnt) + cfg.stall_tx);
           unsigned char* base = smem + (size_t)s * stage_bytes;
           for (int h = 0; h < W; ++h) {
             int pos = c + h;  // c < W and h < W
             pos -= pos >= W ? W : 0;
-            bulk_load(base + h * slot16, static_cast<const uint16_t*>(a.grads[a.order[pos]]) + e0, cnt * 2,
-                      &full[s]);
+            const void* const* rep = a.grads + a.order[pos] * A;  // that worker's A micro-batches
+            for (int q = 0; q < A; ++q)
+              bulk_load(base + (h * A + q) * slot16, static_cast<const uint16_t*>(rep[q]) + e0, cnt * 2, &full[s]);
           }
-          bulk_load(base + W * slot16, a.master[in] + e0, cnt * 4, &full[s]);
-          bulk_load(base + W * slot16 + 4 * E, a.m[in] + e0, cnt * 4, &full[s]);
-          bulk_load(base + W * slot16 + 8 * E, a.v[in] + e0, cnt * 4, &full[s]);
+          bulk_load(base + R * slot16, a.master[in] + e0, cnt * 4, &full[s]);
+          bulk_load(base + R * slot16 + 4 * E, a.m[in] + e0, cnt * 4, &full[s]);
+          bulk_load(base + R * slot16 + 8 * E, a.v[in] + e0, cnt * 4, &full[s]);
         }
       }
       if (ok) {
@@ -213,9 +219,9 @@ __global__ void __launch_bounds__(bulk_threads(SB), 2) fused_bulk_kernel(const _
         if (H.count == 0) break;
         unsigned char* base = smem + (size_t)s * stage_bytes;
         const int64_t e0 = H.start;
-        bulk_store(a.master[out] + e0, base + W * slot16, H.count * 4);
-        bulk_store(a.m[out] + e0, base + W * slot16 + 4 * E, H.count * 4);
-        bulk_store(a.v[out] + e0, base + W * slot16 + 8 * E, H.count * 4);
+        bulk_store(a.master[out] + e0, base + R * slot16, H.count * 4);
+        bulk_store(a.m[out] + e0, base + R * slot16 + 4 * E, H.count * 4);
+        bulk_store(a.v[out] + e0, base + R * slot16 + 8 * E, H.count * 4);
         bulk_store(a.param[out] + e0, base, H.count * 2);
         bulk_commit();
         bulk_wait_read();
@@ -243,8 +249,8 @@ __global__ void __launch_bounds__(bulk_threads(SB), 2) fused_bulk_kernel(const _
       const int groups = H.count / 8;
       for (int g = ct; g < groups; g += kBulkConsumerWarps * 32) {
         float sum[8];
-        zr::unpack8<DT>(*reinterpret_cast<const uint4*>(base + g * 16), sum);
-        if constexpr (WT > 0) {
+        if constexpr (WT > 0 && AT == 1) {
+          zr::unpack8<DT>(*reinterpret_cast<const uint4*>(base + g * 16), sum);
 #pragma unroll
           for (int h = 1; h < WT; ++h) {
             float x[8];
@@ -253,16 +259,23 @@ __global__ void __launch_bounds__(bulk_threads(SB), 2) fused_bulk_kernel(const _
             for (int j = 0; j < 8; ++j) sum[j] = __fadd_rn(sum[j], x[j]);
           }
         } else {
-          for (int h = 1; h < W; ++h) {
-            float x[8];
-            zr::unpack8<DT>(*reinterpret_cast<const uint4*>(base + h * slot16 + g * 16), x);
+          // each worker's micro-batches summed in order, then the workers in ring order
+          for (int h = 0; h < W; ++h) {
+            float w8[8];
+            zr::unpack8<DT>(*reinterpret_cast<const uint4*>(base + (h * A) * slot16 + g * 16), w8);
+            for (int q = 1; q < A; ++q) {
+              float x[8];
+              zr::unpack8<DT>(*reinterpret_cast<const uint4*>(base + (h * A + q) * slot16 + g * 16), x);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) sum[j] = __fadd_rn(sum[j], x[j]);
+              for (int j = 0; j < 8; ++j) w8[j] = __fadd_rn(w8[j], x[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sum[j] = h == 0 ? w8[j] : __fadd_rn(sum[j], w8[j]);
           }
         }
-        float4* ps = reinterpret_cast<float4*>(base + W * slot16) + 2 * g;
-        float4* ms = reinterpret_cast<float4*>(base + W * slot16 + 4 * E) + 2 * g;
-        float4* vs = reinterpret_cast<float4*>(base + W * slot16 + 8 * E) + 2 * g;
+        float4* ps = reinterpret_cast<float4*>(base + R * slot16) + 2 * g;
+        float4* ms = reinterpret_cast<float4*>(base + R * slot16 + 4 * E) + 2 * g;
+        float4* vs = reinterpret_cast<float4*>(base + R * slot16 + 8 * E) + 2 * g;
         if constexpr (SB) {
           const float4 p0 = ps[0], p1 = ps[1], m0 = ms[0], m1 = ms[1], v0 = vs[0], v1 = vs[1];
           float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
@@ -318,12 +331,10 @@ __global__ void __launch_bounds__(bulk_threads(SB), 2) fused_bulk_kernel(const _
 using BulkKernelFn = void (*)(FusedArgs, BulkCfg);
 
 template <int DT, bool SB>
-BulkKernelFn pick_bulk_kernel(int W) {
-  switch (W) {
-    case 2: return fused_bulk_kernel<DT, 2, SB>;
-    case 8: return fused_bulk_kernel<DT, 8, SB>;
-    default: return fused_bulk_kernel<DT, 0, SB>;
-  }
+BulkKernelFn pick_bulk_kernel(int W, int A) {
+  if (A == 1 && W == 2) return fused_bulk_kernel<DT, 2, 1, SB>;
+  if (A == 1 && W == 8) return fused_bulk_kernel<DT, 8, 1, SB>;
+  return fused_bulk_kernel<DT, 0, 0, SB>;
 }
 
 }  // namespace
