@@ -295,16 +295,17 @@ zr_status zr_plan_set_bucket_blocks(zr_plan* p, int max_blocks);
  * one-dimensional bulk copies (cp.async.bulk, this GPU's memory only) completed on mbarriers,
  * keeping `stages` stages in flight, and eight consumer warps compute from shared memory.
  * Both give the same bytes; only speed differs. Bulk staging covers zr_step (and its CUDA
- * graph capture) for plans with A = 1 and 16-bit gradients, and is what zr_plan_create
- * chooses for such a plan when it has at least four waves of tiles (a plan that streams
- * from HBM; automatic shape); other plans, and the other calls, use register staging.
+ * graph capture) for plans with 16-bit gradients (any W and A: a stage holds the W*A
+ * replica slices), and is what zr_plan_create chooses when the automatic shape keeps
+ * stages of 2048 elements (W*A <= 8) and the plan has at least four waves of tiles (a plan
+ * that streams from HBM); other plans, and the other calls, use register staging.
  * stage_elems = 0 and stages = 0 choose a shape that lets two blocks share an SM. Call it
  * between steps; a CUDA graph captured earlier keeps the kernel it captured.
  * Every wait of a bulk-staged step is bounded (2 s); one that gives up skips the step and
  * makes zr_plan_report (and zr_step with a report) return ZR_ERR_TIMEOUT until
  * zr_plan_reset. Errors: ZR_ERR_INVALID (null plan, unknown staging, stage_elems not 0 or a
- * multiple of 8 up to 65536, stages above 4), ZR_ERR_UNSUPPORTED (A > 1, fp32 gradients, a
- * shape that does not fit an SM's shared memory), ZR_ERR_CUDA.
+ * multiple of 8 up to 65536, stages above 4), ZR_ERR_UNSUPPORTED (fp32 gradients, a shape
+ * that does not fit an SM's shared memory), ZR_ERR_CUDA.
  * ZR_STAGING_BULK_IO: as ZR_STAGING_BULK, and the results go out the same way: the consumers
  * write each stage's new master/m/v and 16-bit parameter back into its shared-memory slots
  * and a storer warp copies them to state set 1-k with bulk copies (shared to global). */

@@ -281,14 +281,17 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
     zr_plan_destroy(p);
     return ss;
   }
-  // zr_step stages its loads by bulk copies where that applies (A = 1, 16-bit gradients) and
-  // the plan streams from HBM (at least four waves of tiles): measured 1 % faster than
-  // register staging on both the 7B (W = 2) and 1.3B (W = 8) workloads. A small plan is
+  // zr_step stages its loads by bulk copies where the automatic shape keeps stages of 2048
+  // elements (W * A <= 8: every consumer thread gets one 8-element group per stage) and the
+  // plan streams from HBM (at least four waves of tiles): measured 0.6-1.2 % faster than
+  // register staging on the 7B (W = 2), 1.3B (W = 8) and W = 2, A = 4 workloads. With more
+  // replica slices the stages shrink, consumers sit idle and bulk staging loses (W = 4,
+  // A = 4: 11.9 against 10.6 ms; W = 8, A = 4: 27.5 against 17.4 ms). A small plan is
   // launch-bound, and there the ring's fill costs more than it hides (the 786,432-param
-  // workload: 14.5 us against 12.5 us), so it keeps register staging, as do the plans bulk
-  // staging does not cover.
-  if (p->A == 1 && !p->fp32_grads && p->ntiles > 0) {
-    if (configure_staging(p, ZR_STAGING_BULK, 0, 0) != ZR_OK || p->ntiles < 4 * p->bulk_resident)
+  // workload: 14.5 us against 12.5 us). Those plans keep register staging.
+  if (!p->fp32_grads && p->ntiles > 0) {
+    if (configure_staging(p, ZR_STAGING_BULK, 0, 0) != ZR_OK || p->bulk_E < 2048 ||
+        p->ntiles < 4 * p->bulk_resident)
       p->staging = ZR_STAGING_REGISTERS;
     zr::clear_error();
   }
