@@ -458,8 +458,6 @@ def _measure_other_staging(args, w, zr, plan, hyper, state, grads, dev, stream, 
     into registers), captured as a CUDA graph and timed like the main step on the same buffers; the plan's own
     staging is restored afterwards."""
     import torch
-    if w.A != 1:
-        return None
     own = plan.staging
     other = zr.STAGING_REGISTERS if own == zr.STAGING_BULK else zr.STAGING_BULK
     try:
