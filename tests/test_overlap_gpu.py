@@ -151,10 +151,13 @@ def test_overlapped_schedule_matches_oracle():
                            u16(L["param"]), *o, exact=True, where=f"overlapped step {step}: ")
 
 
-def test_graph_replay_steps_like_direct_calls():
-    """A CUDA graph of one zr_step, replayed, keeps stepping (live set, scale and t come from device memory)
-    and gives the same bytes as calling zr_step each time."""
+@pytest.mark.parametrize("staging", [zr.STAGING_REGISTERS, zr.STAGING_BULK])
+def test_graph_replay_steps_like_direct_calls(staging):
+    """A CUDA graph of one zr_step, replayed (the launch the benchmark times), keeps stepping (live set, scale
+    and t come from device memory) and gives the same bytes as calling zr_step each time, with either load
+    staging in the graph."""
     plans, lay, table, (sa, sb) = _setup(W=2, dtype=zr.BF16, S=1.0)
+    plans[1].set_staging(staging)
     n = plans[0].numel
     grads = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     for r in range(2):
