@@ -1,6 +1,6 @@
 """GPU parity: every C-ABI call against the oracle, element by element, on seeded inputs.
 
-Bar (BASELINE tolerances): reduced sums, overflow flag and skip decision bit-exact; fp32 master/m/v
+Bar (the stated tolerances): reduced sums, overflow flag and skip decision bit-exact; fp32 master/m/v
 within 2 ulp; 16-bit params within 1 ulp. The kernels follow the oracle's op order with IEEE
 round-to-nearest ops and no contraction, so these tests also assert bit-exactness where it is expected.
 """
