@@ -49,3 +49,33 @@ def test_offload_adamw_skips_on_nonfinite(zr):
     for a, b in zip(arrs, before):
         assert a.tobytes() == b.tobytes()
     assert np.all(out == 7)
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_offload_cast_every_boundary(zr, dtype):
+    """The host cast to fp16 / bf16, exhaustively at its boundaries: with lr = weight decay = 0 the update leaves
+    the master as it is (p * 1 - 0 * u), so the 16-bit output is the cast of the input, compared with the oracle's
+    IEEE encoder on every 16-bit value's fp32 image, the midpoints between neighbours and one fp32 ulp on either
+    side of each midpoint (the round-to-nearest-even ties and their neighbours), zeros, infinities, NaNs and the
+    overflow threshold."""
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.decode(dtype, allbits)
+    fin = vals[np.isfinite(vals)].astype(np.float64)
+    fin = np.unique(fin)
+    mids = ((fin[:-1] + fin[1:]) / 2).astype(F32)
+    near = np.concatenate([mids, np.nextafter(mids, np.float32(np.inf)), np.nextafter(mids, np.float32(-np.inf))])
+    specials = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, -np.nan, 65504.0, 65519.99, 65520.0, 3.4e38, -3.4e38,
+                         1e-45, -1e-45, 2.0 ** -25, 2.0 ** -24, 2.0 ** -133, 2.0 ** -134], dtype=F32)
+    p = np.concatenate([vals.astype(F32), near, specials]).astype(F32)
+    n = p.size
+    sums = np.zeros(n, F32)
+    m = np.zeros(n, F32)
+    v = np.zeros(n, F32)
+    out = np.zeros(n, np.uint16)
+    h = zr.AdamW(lr=0.0, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    assert zr.offload_adamw(sums, p, m, v, out, dtype, h, 1.0, 1, 1, 4) == 0
+    want = oracle.encode(dtype, p)
+    nan = np.isnan(p)
+    assert np.array_equal(out[~nan], want[~nan])
+    # NaN: the canonical quiet NaN of its sign
+    assert np.all((out[nan] & 0x7FFF) == (0x7E00 if dtype == 0 else 0x7FC0))
