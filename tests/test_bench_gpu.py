@@ -49,6 +49,23 @@ def test_bench_line_pingpong():
     d = run_bench()
     check_contract(d, 1)
     assert d["inplace_step"]["launches_per_step"] == 2 and d["unfused_chain"]["ms_per_step"] > 0
+    # a plan this small keeps register staging; the other staging is timed beside it
+    assert d["staging"] == "registers" and d["other_staging"]["staging"] == "bulk"
+    assert d["other_staging"]["ms_per_step"] > 0
+
+
+def test_bench_line_second_workload():
+    """The second workload (the default command's 1.3B key, here the GPT-2 shapes) is timed on its own buffers and
+    reported under its own key, with its roofline, the other staging and the no-allocation step beside it."""
+    d = run_bench("--second", "gpt2")
+    check_contract(d, 1)
+    s = d["workload_gpt2"]
+    assert s["config"]["workload"].startswith("gpt2") and s["value"] > 0 and s["ms_per_step"] > 0
+    assert s["config"]["staging"] == "bulk" and s["other_staging"]["staging"] == "registers"
+    r = s["roofline"]
+    assert r["bound"] == "hbm" and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    assert s["noalloc_step"]["ms_per_step"] > 0 and s["noalloc_step"]["zr_step_ms_per_step"] > 0
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(s["clocks"])
 
 
 def test_bench_line_in_place():
