@@ -9,13 +9,14 @@ live set, the loss scale and t from call to call.
 
 Every test here calls the entry point through the C ABI (ctypes on libzr.so) and checks each call bit
 for bit against the oracle, which runs the ring hop by hop on the host, from the oracle's own bucket
-table. The cases cover both specialised kernel widths the workloads use (fp16 W = 2, bf16 W = 8), a
-width without its own instantiation (W = 6), micro-batch accumulation (A = 2), a plan small enough
-that the call halves its tile size, a layout of more than 64 buckets (several set-up launches), a
-skipped step, t far beyond any training run, the empty plan, and a warm call that must not change the
-device's free memory. The file's name sorts last, so a run that stops at the first failure has run
-every other test before it; it also passes alone in a fresh process (it builds the library and makes
-its own inputs).
+table (the large plan against zr_step, itself bit-exact against the oracle in the other test files). The
+cases cover both specialised kernel widths the workloads use (fp16 W = 2, bf16 W = 8), a width without
+its own instantiation (W = 6), micro-batch accumulation (A = 2), a plan small enough that the call
+halves its tile size, a layout of more than 64 buckets (several set-up launches), a skipped step, t far
+beyond any training run, the empty plan, a plan large enough for bulk-copy staging (against zr_step),
+and a warm call that must not change the device's free memory. The file's name sorts last, so a run that
+stops at the first failure has run every other test before it; it also passes alone in a fresh process
+(it builds the library and makes its own inputs).
 """
 import ctypes
 import os
@@ -248,6 +249,30 @@ def test_noalloc_large_t_matches_restored_plan(env):
     for name in ("master", "m", "v", "param"):
         assert torch.equal(ref.live(rep.current)[name].view(torch.int8),
                            run.state.live(1)[name].view(torch.int8)), name
+    plan.close()
+
+
+def test_noalloc_large_plan_matches_bulk_staged_zr_step(env):
+    """A plan large enough to stream from HBM (about 48M params, more than four waves of tiles): the call stages its
+    loads with bulk copies as zr_step does for such a plan, and two calls in a row give zr_step's bytes exactly."""
+    zr = env["zr"]
+    numels = [24_000_000, 3_000, 24_000_000]
+    run = Run(env, numels, 2, 1, zr.F16, 30_000_000, S=1024.0, seed=12)
+    plan = zr.Plan(numels, W=2, A=1, dtype=zr.F16, stage=1, cap=30_000_000, scaler=zr.Scaler(1024.0))
+    assert np.array_equal(plan.buckets, run.buckets) and plan.staging == zr.STAGING_BULK
+    ref = plan.new_state()
+    ref.master[0].copy_(run.state.master[0])
+    ref.param[0].copy_(run.state.param[0])
+    for step in (1, 2):
+        run.fill(step)
+        run.call()
+        rep = plan.step(run.grads, ref, run.hyper, report=True)
+        torch.cuda.synchronize()
+        assert int(run.overflow.item()) == 0 and rep.overflow == 0
+        run.current, run.t = 1 - run.current, run.t + 1
+        for name in ("master", "m", "v", "param"):
+            assert torch.equal(ref.live(rep.current)[name].view(torch.int8),
+                               run.state.live(run.current)[name].view(torch.int8)), f"step {step}: {name}"
     plan.close()
 
 

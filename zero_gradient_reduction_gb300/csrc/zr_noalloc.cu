@@ -33,6 +33,7 @@ using zr::fail;
 
 #include "zr_plan.h"
 #include "zr_step_kernel.cuh"
+#include "zr_step_bulk.cuh"
 
 namespace {
 
@@ -277,8 +278,31 @@ extern "C" zr_status zr_step_noalloc(const zr_bucket* buckets, int nbuckets, int
   a.tiles = reinterpret_cast<const int4*>(static_cast<unsigned char*>(scratch) + kHeaderBytes);
   a.tile0 = 0;
   a.tile1 = ntiles;
+  // The kernel zr_step would use: bulk-copy staging where zr::bulk_preferred says so (it
+  // allocates nothing: its shared memory is an attribute of the kernel, set on this device
+  // here), else register staging.
+  BulkKernelFn bulk = nullptr;
+  BulkCfg cfg{0, 0, 0u};
+  int bulk_smem = 0;
+  {
+    int E = 0, NS = 0;
+    zr::bulk_auto_shape(W * A, &E, &NS);
+    const int smem = NS * bulk_stage_bytes(W * A, E);
+    BulkKernelFn k = dtype == ZR_F16 ? pick_bulk_kernel<zr::DT_F16, false>(W, A)
+                                     : pick_bulk_kernel<zr::DT_BF16, false>(W, A);
+    int bps = 0;
+    cudaError_t eb = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (eb == cudaSuccess) eb = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, k, bulk_threads(false), smem);
+    if (eb != cudaSuccess) (void)cudaGetLastError();  // not fatal: register staging then
+    else if (bps > 0 && zr::bulk_preferred(E, ntiles, (int64_t)sms * bps)) {
+      bulk = k;
+      cfg.E = E;
+      cfg.NS = NS;
+      bulk_smem = smem;
+    }
+  }
   const int grid = (int)(ntiles >= 4 * full ? ntiles : (ntiles < full ? ntiles : full));
-  a.total_blocks = (unsigned)grid;
+  a.total_blocks = (unsigned)(bulk ? ntiles : grid);
   for (int k = 0; k < 2; ++k) {
     a.master[k] = st->master[k];
     a.m[k] = st->m[k];
@@ -294,7 +318,8 @@ extern "C" zr_status zr_step_noalloc(const zr_bucket* buckets, int nbuckets, int
   a.W = W;
   a.A = A;
   a.stage = 1;
-  kern<<<grid, kThreads, 0, cs>>>(a);
+  if (bulk) bulk<<<(int)ntiles, bulk_threads(false), bulk_smem, cs>>>(a, cfg);
+  else kern<<<grid, kThreads, 0, cs>>>(a);
   e = cudaGetLastError();
   // the step's flag, which its last block leaves in the control block, to the caller
   if (e == cudaSuccess)

@@ -59,6 +59,13 @@ namespace zr {
 zr_status build_shard_tables(zr_plan* p);
 // Picks the in-place step's kernels and grids once the tile table exists (zr_inplace.cu).
 zr_status init_inplace(zr_plan* p);
+// The automatic stage shape of bulk-copy staging for R = W*A replica slices (zr_step.cu):
+// fills *E if it is 0 and *NS if it is 0.
+void bulk_auto_shape(int R, int* E, int* NS);
+// Whether the automatic shape suits a step of R replica slices over ntiles tiles when
+// `resident` blocks of the bulk kernel fit on the GPU at once: stages of 2048 elements
+// and at least four waves of tiles (the rule zr_plan_create and zr_step_noalloc apply).
+bool bulk_preferred(int E, int64_t ntiles, int64_t resident);
 
 // Blocks for a launch over `ntiles` tiles. A large launch gets one block per tile: the
 // hardware hands blocks out in index order as earlier ones finish, so the tiles in flight

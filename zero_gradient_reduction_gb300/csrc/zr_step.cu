@@ -69,6 +69,33 @@ static void set_bucket_grids(zr_plan* p, int max_blocks) {
   }
 }
 
+// Automatic shape: two blocks per SM (at most kBulkBudget of shared memory each, which with
+// the per-block reserve fills an SM's 228 KB), stages of 2048 elements (one 8-element group
+// per consumer thread) where two of them fit, else smaller; as many stages as the budget
+// holds, up to kBulkMaxStages. Measured on the 7B (W = 2) and 1.3B (W = 8) workloads:
+// 2048 x 3 and 2048 x 2 beat every other shape, and smaller stages (1024) or one block per
+// SM (4096) lose 10-25 %.
+void zr::bulk_auto_shape(int R, int* E, int* NS) {
+  constexpr int kBulkBudget = 113 * 1024;
+  if (*E == 0) {
+    *E = 2048;
+    while (*E > 256 && 2 * bulk_stage_bytes(R, *E) > kBulkBudget) *E /= 2;
+  }
+  if (*NS == 0) {  // a stage larger than the budget (hundreds of replica slices) runs alone on its SM
+    const int ns = kBulkBudget / bulk_stage_bytes(R, *E);
+    *NS = ns < 1 ? 1 : ns > kBulkMaxStages ? kBulkMaxStages : ns;
+  }
+}
+
+// Bulk staging is chosen where the automatic shape keeps stages of 2048 elements (W * A <=
+// 8: every consumer thread gets one 8-element group per stage) and the plan streams from HBM
+// (at least four waves of tiles): measured 0.6-1.2 % faster than register staging on the 7B
+// (W = 2), 1.3B (W = 8) and W = 2, A = 4 workloads. With more replica slices the stages
+// shrink, consumers sit idle and bulk staging loses (W = 4, A = 4: 11.9 against 10.6 ms;
+// W = 8, A = 4: 27.5 against 17.4 ms). A small plan is launch-bound, and there the ring's
+// fill costs more than it hides (the 786,432-param workload: 14.5 us against 12.5 us).
+bool zr::bulk_preferred(int E, int64_t ntiles, int64_t resident) { return E >= 2048 && ntiles >= 4 * resident; }
+
 // Chooses how zr_step stages its loads (the body of zr_plan_set_staging; zr_plan_create
 // also calls it to make bulk staging the default where it applies).
 static zr_status configure_staging(zr_plan* p, int staging, int stage_elems, int stages) {
@@ -85,22 +112,8 @@ static zr_status configure_staging(zr_plan* p, int staging, int stage_elems, int
     return fail(ZR_ERR_INVALID, "zr_plan_set_staging: stage_elems must be 0 or a multiple of 8 up to 65536");
   if (stages < 0 || stages > kBulkMaxStages)
     return fail(ZR_ERR_INVALID, "zr_plan_set_staging: stages must be 0 or 1..%d", kBulkMaxStages);
-  // Automatic shape: two blocks per SM (at most kBulkBudget of shared memory each, which
-  // with the per-block reserve fills an SM's 228 KB), stages of 2048 elements (one 8-element
-  // group per consumer thread) where two of them fit, else smaller; as many stages as the
-  // budget holds, up to kBulkMaxStages. Measured on the 7B (W = 2) and 1.3B (W = 8)
-  // workloads: 2048 x 3 and 2048 x 2 beat every other shape, and smaller stages (1024) or
-  // one block per SM (4096) lose 10-25 %.
-  constexpr int kBulkBudget = 113 * 1024;
   int E = stage_elems, NS = stages;
-  if (E == 0) {
-    E = 2048;
-    while (E > 256 && 2 * bulk_stage_bytes(R, E) > kBulkBudget) E /= 2;
-  }
-  if (NS == 0) {  // a stage larger than the budget (hundreds of replica slices) runs alone on its SM
-    NS = kBulkBudget / bulk_stage_bytes(R, E);
-    NS = NS < 1 ? 1 : NS > kBulkMaxStages ? kBulkMaxStages : NS;
-  }
+  zr::bulk_auto_shape(R, &E, &NS);
   const int64_t smem64 = (int64_t)NS * bulk_stage_bytes(R, E);
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
@@ -281,17 +294,11 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
     zr_plan_destroy(p);
     return ss;
   }
-  // zr_step stages its loads by bulk copies where the automatic shape keeps stages of 2048
-  // elements (W * A <= 8: every consumer thread gets one 8-element group per stage) and the
-  // plan streams from HBM (at least four waves of tiles): measured 0.6-1.2 % faster than
-  // register staging on the 7B (W = 2), 1.3B (W = 8) and W = 2, A = 4 workloads. With more
-  // replica slices the stages shrink, consumers sit idle and bulk staging loses (W = 4,
-  // A = 4: 11.9 against 10.6 ms; W = 8, A = 4: 27.5 against 17.4 ms). A small plan is
-  // launch-bound, and there the ring's fill costs more than it hides (the 786,432-param
-  // workload: 14.5 us against 12.5 us). Those plans keep register staging.
+  // zr_step stages its loads by bulk copies where zr::bulk_preferred says so; other plans
+  // keep register staging.
   if (!p->fp32_grads && p->ntiles > 0) {
-    if (configure_staging(p, ZR_STAGING_BULK, 0, 0) != ZR_OK || p->bulk_E < 2048 ||
-        p->ntiles < 4 * p->bulk_resident)
+    if (configure_staging(p, ZR_STAGING_BULK, 0, 0) != ZR_OK ||
+        !zr::bulk_preferred(p->bulk_E, p->ntiles, p->bulk_resident))
       p->staging = ZR_STAGING_REGISTERS;
     zr::clear_error();
   }
