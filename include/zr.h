@@ -465,7 +465,9 @@ zr_status zr_offload_step(zr_plan* p, int stage, const void* const* grads, float
  * which a caller cannot accept if its runtime owns all device memory through its own
  * pool, if its memory budget was fixed before the first step, or if an allocation
  * would synchronise the device on its path. zr_step_noalloc computes exactly what
- * zr_step computes for one step, allocating nothing (no cudaMalloc, no cudaFree, no
+ * zr_step computes for one step, with the kernel zr_step would choose for these buckets
+ * (bulk-copy staging, whose shared memory is a kernel attribute set on the current
+ * device, or register staging), allocating nothing (no cudaMalloc, no cudaFree, no
  * allocating library routine): its scratch is one static device array of this library
  * (ZR_NOALLOC_MAX_TILES tiles plus a 256-byte control block), present on every GPU that loads
  * the library until the process exits.
