@@ -44,9 +44,18 @@ def test_random_plan_matches_oracle(case):
     dynamic = bool(rng.integers(0, 2))
     sigma = rng.uniform(1e-3, 1e-1, size=ntensors)
     cls = InPlaceRun if rng.integers(0, 2) else FusedRun
-    # the plan's own staging, or one chosen
+    # the plan's own staging, or one chosen; a bulk staging half of the time with a drawn stage shape (stages of
+    # 256-4096 elements, 1-4 of them, as long as they fit a block's shared memory)
     pick = int(rng.integers(0, 4))
     staging = None if pick == 0 else ((zr.STAGING_REGISTERS, zr.STAGING_BULK, zr.STAGING_BULK_IO)[pick - 1], 0, 0)
+    if pick >= 2 and rng.integers(0, 2):
+        E = int(rng.choice([256, 512, 1024, 2048, 4096]))
+        NS = int(rng.integers(1, 5))
+        while NS > 1 and NS * (2 * W * A * E + 12 * E) > 200 * 1024:
+            NS -= 1
+        while E > 256 and NS * (2 * W * A * E + 12 * E) > 200 * 1024:
+            E //= 2
+        staging = (staging[0], E, NS)
     run = cls(numels, W, A, dtype, cap=cap, S=S, dynamic=dynamic, order=order, seed=case, sigma=sigma,
               interval=2, staging=staging)
     where = f"case {case}: W={W} A={A} dtype={dtype} cap={cap} numels={numels} {cls.__name__}"
