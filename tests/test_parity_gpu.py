@@ -345,9 +345,11 @@ def test_fused_ragged_buckets(W, A, dtype, staging):
         run.check(f"W={W} A={A} step {s}: ")
 
 
-def test_fused_skip_then_resume():
+@pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
+def test_fused_skip_then_resume(staging):
     numels = [20_000, 4_000, 30_000]
-    run = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=5)
+    run = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=5,
+                   staging=None if staging is None else (staging, 0, 0))
     run.step(1)
     before = [x.copy() for x in run.live()]
     cur = run.current
@@ -362,8 +364,10 @@ def test_fused_skip_then_resume():
         run.check(f"resume step {s}: ")
 
 
-def test_fused_scale_growth():
-    run = FusedRun([4096, 1000], 2, 1, zr.BF16, cap=10_000, S=4.0, dynamic=True, interval=2)
+@pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
+def test_fused_scale_growth(staging):
+    run = FusedRun([4096, 1000], 2, 1, zr.BF16, cap=10_000, S=4.0, dynamic=True, interval=2,
+                   staging=None if staging is None else (staging, 0, 0))
     scales = []
     for s in range(1, 6):
         rep, _ = run.step(s)
@@ -372,11 +376,13 @@ def test_fused_scale_growth():
     run.check()
 
 
-def test_default_growth_interval_over_a_thousand_steps():
+@pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
+def test_default_growth_interval_over_a_thousand_steps(staging):
     """The default rule (growth after 1000 clean steps) run to its first growth: the scale doubles on step
     1001 exactly, a skip at step 1003 halves it and resets the count, and the state after 1005 steps is the
-    oracle's, bit for bit."""
-    run = FusedRun([2048, 1000], 2, 1, zr.F16, cap=4096, S=1024.0, dynamic=True, seed=13, interval=1000)
+    oracle's, bit for bit (register staging, the plan's own for this size, and bulk-copy staging)."""
+    run = FusedRun([2048, 1000], 2, 1, zr.F16, cap=4096, S=1024.0, dynamic=True, seed=13, interval=1000,
+                   staging=None if staging is None else (staging, 0, 0))
     for s in range(1, 1006):
         rep, _ = run.step(s, inject=(1, 5) if s == 1003 else None)
         if s <= 1000:
@@ -391,11 +397,13 @@ def test_default_growth_interval_over_a_thousand_steps():
     run.check("after 1005 steps: ")
 
 
-def test_stages_identical():
+@pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
+def test_stages_identical(staging):
     """DDP (stage 0) and ZeRO stages 1-3 give the same bytes."""
     outs = []
     for stage in (0, 1, 2, 3):
-        run = FusedRun([70_000, 5000], 4, 1, zr.BF16, cap=50_000, S=1.0, seed=11, stage=stage)
+        run = FusedRun([70_000, 5000], 4, 1, zr.BF16, cap=50_000, S=1.0, seed=11, stage=stage,
+                       staging=None if staging is None else (staging, 0, 0))
         for s in (1, 2):
             rep, _ = run.step(s, stage=stage)
             assert rep.stage == stage
@@ -455,21 +463,24 @@ def test_error_paths():
     assert r.t == 1 and r.overflow == 0
 
 
-def test_checkpoint_resume_is_byte_identical():
+@pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
+def test_checkpoint_resume_is_byte_identical(staging):
     """Run 4 steps straight; separately run 2, checkpoint (control block + live state), restore into a fresh
     plan and state, run steps 3-4: the live state matches byte for byte, with a skip in between."""
     numels = [30_000, 5_000, 17_000]
-    straight = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=9, interval=2)
+    stg = None if staging is None else (staging, 0, 0)
+    straight = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=9, interval=2,
+                        staging=stg)
     inj = (0, int(straight.ooffsets[1]) + 7)
     for s in range(1, 5):
         straight.step(s, inject=inj if s == 2 else None)
-    first = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=9, interval=2)
+    first = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=9, interval=2, staging=stg)
     for s in (1, 2):
         first.step(s, inject=inj if s == 2 else None)
     ck = first.plan.checkpoint()
     saved = {k: v.clone() for k, v in first.state.live(ck.current).items()}
     assert ck.t == 1 and ck.skipped == 1 and ck.scale == 32768.0
-    second = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=9, interval=2)
+    second = FusedRun(numels, 2, 1, zr.F16, cap=25_000, S=65536.0, dynamic=True, seed=9, interval=2, staging=stg)
     second.plan.restore(ck)
     live = second.state.live(ck.current)
     for k in saved:
