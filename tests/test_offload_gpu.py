@@ -1,4 +1,4 @@
-"""ZeRO-Offload step on the GPU machine: reduce-scatter on the GPU, AdamW on the host CPU over host-resident
+"""ZeRO-Offload step: reduce-scatter on the GPU, AdamW on the host CPU over host-resident
 master/m/v, parameters back to the device. Checked against the oracle bit for bit, including a skip."""
 import numpy as np
 import pytest

@@ -3,7 +3,7 @@
 The pages fix the order (page "DP / DDP / DeepSpeed ZeRO-1/2/3", section 二: parameters are laid out in the
 reverse of their definition order, output layer first, and synchronised one full bucket at a time; page
 "第 7 讲：Parallelism（上）", DDP 核心实现细节 3: buckets follow the reverse of the backward order). The
-cap rule is this build's reading: a non-empty bucket closes before a tensor that would take it past the cap.
+cap rule is the reading taken here: a non-empty bucket closes before a tensor that would take it past the cap.
 The counts below follow from that reading and the shape lists by hand arithmetic (e.g. GPT-2: three layers
 (21.24M) + norm_b + norm_a + fc2 = 23.60M; adding fc1 would pass 25M).
 """
