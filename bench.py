@@ -245,7 +245,7 @@ def _config(w, buckets, l2_note, launch=None, inplace=False):
 
 
 def measure_overlap(torch, zr, plan, grads, state, hyper, dev, stream, tokens: int = 8192, reps: int = 3,
-                    budget_caps=(16, 38, 76, 152, 304)):
+                    budget_caps=(16, 38, 76, 152, 304), step_bytes=None):
     """Bucketed overlap against a synthetic backward: on a compute stream, bucket b's "backward" is a bf16 GEMM
     of about 4 * tokens * n_b FLOPs (weight and input gradients of n_b parameters), after which an event marks
     the bucket's gradients ready and zr_step_bucket(b) runs on a side stream. Compared with backward followed by
@@ -291,19 +291,29 @@ def measure_overlap(torch, zr, plan, grads, state, hyper, dev, stream, tokens: i
     def step_only():
         plan.step(grads, state, hyper, stream=stream)
 
+    def buckets_only():
+        for b in range(len(plan.buckets)):
+            plan.step_bucket(b, grads, state, hyper, stream=side)
+        compute.wait_stream(side)
+
     for fn in (backward, step_only, serial, overlapped):
         fn()
     t_bwd, t_step = timed(backward), timed(step_only)
     t_serial, t_over = timed(serial), timed(overlapped)
     # the same overlap with every bucket launch capped at a block budget (zr_plan_set_bucket_blocks), as a
-    # communication library keeps to a few SMs; 0 = uncapped (one block per tile)
+    # communication library keeps to a few SMs; 0 = uncapped (one block per tile). Beside each, the bucket
+    # launches alone at that budget: the step's rate per block, i.e. how many SMs it needs to keep HBM busy.
     budgets = {}
     for cap in budget_caps:
         plan.set_bucket_blocks(cap)
+        buckets_only()
+        t_alone = timed(buckets_only)
         overlapped()
         t_cap = timed(overlapped)
         budgets[str(cap)] = {"overlapped_ms": t_cap,
-                             "hidden_fraction_of_step": (t_serial - t_cap) / t_step if t_step > 0 else None}
+                             "hidden_fraction_of_step": (t_serial - t_cap) / t_step if t_step > 0 else None,
+                             "step_alone_ms": t_alone,
+                             "step_alone_GBs_per_block": (step_bytes / t_alone / 1e6 / cap) if step_bytes else None}
     plan.set_bucket_blocks(0)
     return {"backward_ms": t_bwd, "step_ms": t_step, "serial_ms": t_serial, "overlapped_ms": t_over,
             "hidden_fraction_of_step": (t_serial - t_over) / t_step if t_step > 0 else None,
@@ -709,7 +719,7 @@ def run_zr(args, w):
 
     overlap = None
     if side and w.A == 1:
-        overlap = measure_overlap(torch, zr, plan, grads, state, hyper, dev, stream)
+        overlap = measure_overlap(torch, zr, plan, grads, state, hyper, dev, stream, step_bytes=step_bytes)
 
     offload = None
     if side and w.A == 1 and ws == 1:

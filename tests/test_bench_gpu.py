@@ -52,6 +52,10 @@ def test_bench_line_pingpong():
     # a plan this small keeps register staging; the other staging is timed beside it
     assert d["staging"] == "registers" and d["other_staging"]["staging"] == "bulk"
     assert d["other_staging"]["ms_per_step"] > 0
+    o = d["bucketed_overlap"]
+    assert o["serial_ms"] > 0 and o["overlapped_ms"] > 0
+    for cap in ("16", "152"):
+        assert o["block_budget_sweep"][cap]["step_alone_ms"] > 0 and o["block_budget_sweep"][cap]["overlapped_ms"] > 0
 
 
 def test_bench_line_second_workload():
