@@ -36,11 +36,15 @@ def test_offload_adamw_bit_exact(zr, dtype, nthreads):
         assert np.array_equal(out, oracle.encode(dtype, want[0]))
 
 
-def test_offload_adamw_skips_on_nonfinite(zr):
+@pytest.mark.parametrize("bad", [np.nan, np.inf, -np.inf])
+@pytest.mark.parametrize("where", [0, 37_499, 37_500, 123_456, 299_999])
+def test_offload_adamw_skips_on_nonfinite(zr, bad, where):
+    """One non-finite sum anywhere (the first and last element of a thread's slice of 37,500, the last element)
+    skips the whole update: nothing is written."""
     n = 300_000
     rng = np.random.default_rng(1)
     sums = rng.normal(size=n).astype(F32)
-    sums[123_456] = np.nan
+    sums[where] = bad
     arrs = [rng.normal(size=n).astype(F32) for _ in range(3)]
     arrs[2] = np.abs(arrs[2])
     before = [a.copy() for a in arrs]

@@ -83,10 +83,12 @@ void update_slice(const float* sums, float* p, float* m, float* v, uint16_t* out
   }
 }
 
+// Any +-inf or NaN in x[lo, hi): an all-ones exponent. The test is OR-ed into a 32-bit word, which the
+// compiler vectorises (a bool accumulator it does not: 12.6 against 7.9 ms for 4e8 values on 16 Grace cores).
 bool any_nonfinite(const float* x, int64_t lo, int64_t hi) {
-  bool bad = false;
-  for (int64_t i = lo; i < hi; ++i) bad |= ((f32_bits(x[i]) & 0x7F800000u) == 0x7F800000u);
-  return bad;
+  uint32_t acc = 0;
+  for (int64_t i = lo; i < hi; ++i) acc |= (uint32_t)((f32_bits(x[i]) & 0x7F800000u) == 0x7F800000u);
+  return acc != 0;
 }
 
 template <typename F>
