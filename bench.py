@@ -741,8 +741,9 @@ def run_zr(args, w):
                               w.init_scale, 2 + i, nthreads, stream=stream)
         torch.cuda.synchronize(dev)
         o_ms = (time.perf_counter() - t0) / 2 * 1e3
-        # the host-side bounds of that step: the host AdamW alone (zr_offload_adamw: 4 + 12 bytes read, 12 + 2
-        # written per param of host memory) on the same arrays, and a plain multi-threaded host copy
+        # the host-side bounds of that step: the host AdamW alone (zr_offload_adamw: a flag pass reading the 4-byte
+        # sums, then 4 + 12 bytes read and 12 + 2 written per param of host memory) on the same arrays, and a
+        # plain multi-threaded host copy
         t0 = time.perf_counter()
         zr.offload_adamw(sums_host, h_master, h_m, h_v, param_host, w.dtype, hyper, w.init_scale, w.W, 4, nthreads)
         ha_s = time.perf_counter() - t0
@@ -756,10 +757,14 @@ def run_zr(args, w):
         hc_s = (time.perf_counter() - t0) / 3
         offload = {"ms_per_step": o_ms, "Gparams_per_s": plan.n_real / o_ms / 1e6, "host_threads": nthreads,
                    "link_bytes_per_param": 6, "host_state_GB": 12 * n / 1e9,
-                   "host_adamw_ms": ha_s * 1e3, "host_adamw_GBs": 30 * n / ha_s / 1e9,
+                   # host memory per param and step: the update's 16 read + 14 written, the sums copied in (4)
+                   # and the parameters copied out (2)
+                   "host_bytes_per_param": 36, "host_GBs": 36 * n / o_ms / 1e6,
+                   "host_adamw_ms": ha_s * 1e3, "host_adamw_GBs": 34 * n / ha_s / 1e9,
                    "host_copy_GBs": 8 * k / hc_s / 1e9, "host_copy_threads": torch.get_num_threads(),
                    "call": "zr_offload_step (reduce-scatter on GPU, AdamW on the host CPU, params back); "
-                           "host_adamw: zr_offload_adamw alone on the same host arrays (30 B/param of host memory); "
+                           "host_adamw: zr_offload_adamw alone on the same host arrays (its flag pass over the sums, "
+                           "then the update: 34 B/param of host memory); "
                            "host_copy: torch CPU copy_ of 4 GB fp32 (read + write bytes)"}
         del src, dst
         del sums_dev, sums_host, param_host, h_master, h_m, h_v

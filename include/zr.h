@@ -441,9 +441,10 @@ zr_status zr_offload_adamw(const float* sums, float* master, float* m, float* v,
  * bucket: the sums copied into sums_host (pinned host fp32), the update on the CPU of
  * the host-resident master/m/v (host fp32) into param_host (pinned host, plan dtype),
  * and the parameters copied into param_dev (device replica). The host update of bucket
- * b overlaps the copies of the other buckets. The last parameter copies are still
- * queued on `stream` at return: synchronise it before reading param_dev or reusing
- * param_host. The caller applies its loss-scale rule from *overflow (host int32).
+ * b overlaps the copies of the other buckets. "Pinned" means page-locked: allocated by
+ * cudaHostAlloc or registered with cudaHostRegister. The last parameter copies are
+ * still queued on `stream` at return: synchronise it before reading param_dev or
+ * reusing param_host. The caller applies its loss-scale rule from *overflow (host int32).
  * Errors: ZR_ERR_INVALID for null or misaligned buffers, stage, t < 1, betas outside
  * [0, 1); ZR_ERR_UNSUPPORTED for A > 1; ZR_ERR_CUDA. */
 zr_status zr_offload_step(zr_plan* p, int stage, const void* const* grads, float* sums_dev, float* sums_host,

@@ -24,8 +24,19 @@ def _gpu():
     torch.cuda.set_device(0)
 
 
-@pytest.mark.parametrize("W,dtype", [(2, zr.F16), (4, zr.BF16)])
-def test_offload_step_matches_oracle(W, dtype):
+def _pinned(n, np_dtype, tdt, kind, keep):
+    """A page-locked host buffer: from cudaHostAlloc (torch's pin_memory), or pageable numpy memory registered
+    with cudaHostRegister (kept in `keep` for unregistering)."""
+    if kind == "alloc":
+        return torch.empty(n, dtype=tdt, pin_memory=True)
+    a = np.zeros(n, np_dtype)
+    assert int(torch.cuda.cudart().cudaHostRegister(a.ctypes.data, a.nbytes, 0)) == 0
+    keep.append(a)
+    return torch.from_numpy(a).view(tdt)
+
+
+@pytest.mark.parametrize("W,dtype,kind", [(2, zr.F16, "alloc"), (4, zr.BF16, "alloc"), (2, zr.BF16, "registered")])
+def test_offload_step_matches_oracle(W, dtype, kind):
     numels = [300_000, 999, 120_000, 64]
     S = 1024.0 if dtype == zr.F16 else 1.0
     plan = zr.Plan(numels, W=W, dtype=dtype, stage=2, cap=200_000, order=list(range(W))[::-1])
@@ -37,10 +48,11 @@ def test_offload_step_matches_oracle(W, dtype):
     tdt = plan.torch_dtype()
     grads = [torch.zeros(n, dtype=tdt, device="cuda") for _ in range(W)]
     sums_dev = torch.empty(n, dtype=torch.float32, device="cuda")
-    sums_host = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    keep = []
+    sums_host = _pinned(n, F32, torch.float32, kind, keep)
     master = lay.master_host(0, n)
     m, v = np.zeros(n, F32), np.zeros(n, F32)
-    param_host = torch.empty(n, dtype=tdt, pin_memory=True)
+    param_host = _pinned(n, np.uint16, tdt, kind, keep)
     param_dev = torch.zeros(n, dtype=tdt, device="cuda")
     o = [master.copy(), m.copy(), v.copy(), np.zeros(n, np.uint16)]
     osc = oracle.new_scaler(S, dynamic=True)
@@ -67,6 +79,9 @@ def test_offload_step_matches_oracle(W, dtype):
             assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
         assert np.array_equal(u16(param_dev), o[3])
     plan.close()
+    torch.cuda.synchronize()
+    for a in keep:
+        assert int(torch.cuda.cudart().cudaHostUnregister(a.ctypes.data)) == 0
 
 
 @pytest.mark.parametrize("case", range(8))
