@@ -385,7 +385,7 @@ typedef struct {
 zr_status zr_plan_checkpoint(zr_plan* p, void* stream, zr_checkpoint* out);
 /* Writes *in into the control block on `stream` and synchronises it.
  * Errors: ZR_ERR_INVALID for a null argument, current not 0/1, a scale that is not
- * positive and finite, negative counters. */
+ * positive and finite, negative counters, beta powers outside [0, 1]. */
 zr_status zr_plan_restore(zr_plan* p, const zr_checkpoint* in, void* stream);
 
 /* ------------------------------------------------------------------------- */
@@ -484,7 +484,9 @@ zr_status zr_offload_step(zr_plan* p, int stage, const void* const* grads, float
  * per call and any t costs at most the walk to the products' fixed point. overflow:
  * device int32, set to 1 if any reduced gradient is not finite, else 0 (also 0 for an
  * empty bucket table); when it is 1 the written set must be discarded (keep `current`),
- * and the caller applies its own loss-scale rule.
+ * and the caller applies its own loss-scale rule. Under bulk-copy staging a wait that
+ * gave up (each is bounded at 2 s; zr_step reports that as ZR_ERR_TIMEOUT) also sets
+ * it to 1: nothing is lost, but this call cannot tell it from an overflow.
  * The caller carries the live-set index, the scale and t between calls.
  *
  * Every call on a device reuses the same scratch and leaves its last contents there;

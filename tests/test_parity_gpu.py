@@ -494,9 +494,11 @@ def test_checkpoint_resume_is_byte_identical(staging):
     for a, b in zip(straight.live(), second.live()):
         assert a.tobytes() == b.tobytes()
     second.check("resumed: ")
-    with pytest.raises(zr.ZrError):
-        bad = zr.Checkpoint(2, 1.0, 0, 0, 0, 0, 1.0, 1.0)
-        second.plan.restore(bad)
+    for bad in (zr.Checkpoint(2, 1.0, 0, 0, 0, 0, 1.0, 1.0), zr.Checkpoint(0, 0.0, 0, 0, 0, 0, 1.0, 1.0),
+                zr.Checkpoint(0, 1.0, -1, 0, 0, 0, 1.0, 1.0), zr.Checkpoint(0, 1.0, 0, 0, 0, 0, 1.5, 1.0),
+                zr.Checkpoint(0, 1.0, 0, 0, 0, 0, 0.5, float("nan")), zr.Checkpoint(0, 1.0, 0, 0, 0, 0, -0.1, 0.9)):
+        with pytest.raises(zr.ZrError):
+            second.plan.restore(bad)
 
 
 # ----------------------------------------------------------------------------- bulk-copy staging

@@ -390,6 +390,9 @@ extern "C" zr_status zr_plan_restore(zr_plan* p, const zr_checkpoint* in, void* 
     return fail(ZR_ERR_INVALID, "zr_plan_restore: scale must be positive and finite");
   if (in->good < 0 || in->t < 0 || in->steps < 0 || in->skipped < 0)
     return fail(ZR_ERR_INVALID, "zr_plan_restore: negative counter");
+  // running products of betas in [0, 1): a value outside [0, 1] (or NaN) is no such product
+  if (!(in->beta1_pow >= 0.0 && in->beta1_pow <= 1.0) || !(in->beta2_pow >= 0.0 && in->beta2_pow <= 1.0))
+    return fail(ZR_ERR_INVALID, "zr_plan_restore: beta powers must lie in [0, 1]");
   zr::Ctrl c = initial_ctrl(p->scaler);
   c.k = in->current;
   c.scale = in->scale;
