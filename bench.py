@@ -323,27 +323,56 @@ def measure_overlap(torch, zr, plan, grads, state, hyper, dev, stream, tokens: i
                    "bucket launch with zr_plan_set_bucket_blocks"}
 
 
-def _link_rates(torch, host, dev_buf, dev, stream, max_bytes: int = 4 << 30, reps: int = 3):
-    """Host<->device copy bandwidth: `reps` copies of up to max_bytes between a pinned host tensor and a device
-    tensor, each direction timed with CUDA events on the launching stream."""
+def _host_memory_short(bytes_per_rank: int, local_ranks: int):
+    """None if the host has room to pin bytes_per_rank for each of this node's ranks (with a tenth to spare), else
+    the reason it has not (read from /proc/meminfo; unknown counts as room)."""
+    try:
+        with open("/proc/meminfo") as f:
+            avail = next(int(l.split()[1]) * 1024 for l in f if l.startswith("MemAvailable:"))
+    except (OSError, StopIteration, ValueError):
+        return None
+    need = int(1.1 * bytes_per_rank * local_ranks)
+    if avail >= need:
+        return None
+    return (f"host memory: {local_ranks} rank(s) x {bytes_per_rank / 1e9:.1f} GB of pinned gradients need "
+            f"{need / 1e9:.0f} GB, {avail / 1e9:.0f} GB available")
+
+
+def _e2e_host_memory_short(bytes_per_rank: int, ws: int, device=None):
+    """Whether the end-to-end leg must be left out for want of host memory to pin each rank's gradients: the
+    reason, or None. Every rank takes the same decision, since the leg has a barrier and a max over ranks."""
+    short = _host_memory_short(bytes_per_rank, int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
+    if max_over_ranks(1.0 if short else 0.0, ws, device) > 0.0 and not short:
+        short = "host memory: another rank of this job has too little to pin its gradients"
+    return short
+
+
+def _link_rates(torch, host, dev_buf, dev, stream, max_bytes: int = 4 << 30, reps: int = 3, rounds: int = 3):
+    """Host<->device copy bandwidth: `rounds` rounds of `reps` copies of up to max_bytes between a pinned host
+    tensor and a device tensor, each direction timed with CUDA events on the launching stream; the best round
+    counts (the link is shared with the host's other traffic, so single rounds vary)."""
     k = min(host.numel(), dev_buf.numel(), max_bytes // host.element_size())
     h, d = host[:k], dev_buf[:k]
     nbytes = k * host.element_size()
     out = {}
     for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        best = 0.0
         with torch.cuda.stream(stream):
             dst.copy_(src, non_blocking=True)
             torch.cuda.synchronize(dev)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(reps):
-                dst.copy_(src, non_blocking=True)
-            e1.record(stream)
-        torch.cuda.synchronize(dev)
-        out[f"link_{name}_GBs"] = nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+            for _ in range(rounds):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    dst.copy_(src, non_blocking=True)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                best = max(best, nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+        out[f"link_{name}_GBs"] = best
     out["link_copy_bytes"] = int(nbytes)
-    out["link_how"] = "pinned host <-> device tensor copy_ (one cudaMemcpyAsync), CUDA events, best-effort single stream"
+    out["link_how"] = (f"pinned host <-> device tensor copy_ (one cudaMemcpyAsync), CUDA events, best of {rounds} "
+                       f"rounds of {reps} copies, single stream")
     return out
 
 
@@ -771,7 +800,10 @@ def run_zr(args, w):
 
     e2e = None
     cpu = None
-    if not args.no_e2e:
+    e2e_short = None if args.no_e2e else _e2e_host_memory_short(2 * n * w.W * w.A, ws, dev)
+    if not args.no_e2e and e2e_short:
+        e2e = {"unavailable": e2e_short}
+    elif not args.no_e2e:
         # end to end through the public API: pinned host gradients copied in every step, report read back
         host = [torch.empty(n, dtype=plan.torch_dtype(), pin_memory=True) for _ in range(w.W * w.A)]
         for r in range(w.W * w.A):

@@ -33,6 +33,41 @@ def _worker(rank, ws, port, q):
     dist.destroy_process_group()
 
 
+def _short_worker(rank, ws, port, q):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(ws))
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    import bench
+    # rank 1 asks for more host memory than any machine has; rank 0 for one byte
+    q.put((rank, bench._e2e_host_memory_short(1 if rank == 0 else 10**18, ws)))
+    dist.destroy_process_group()
+
+
+def test_e2e_host_memory_decision_is_collective_gloo():
+    """A rank that cannot pin its gradients leaves the end-to-end leg out on every rank, so no rank waits at
+    that leg's barrier for one that skipped it."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_short_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert out[1].startswith("host memory:") and "GB available" in out[1]
+    assert out[0] == "host memory: another rank of this job has too little to pin its gradients"
+
+
+def test_host_memory_short_alone():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench._e2e_host_memory_short(1, 1) is None
+    assert bench._host_memory_short(10**18, 1).startswith("host memory: 1 rank(s)")
+
+
 def test_max_over_ranks_and_whole_job_rate_gloo():
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
