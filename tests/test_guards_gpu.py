@@ -61,6 +61,59 @@ def test_guards_fused_step_and_bucketed():
         plan.close()
 
 
+def _guarded_state(n, tdt):
+    st = zr.State.__new__(zr.State)
+    parts = {k: [Guarded(n, torch.float32) for _ in range(2)] for k in ("master", "m", "v")}
+    prm = [Guarded(n, tdt) for _ in range(2)]
+    st.master = [p.t for p in parts["master"]]
+    st.m = [p.t for p in parts["m"]]
+    st.v = [p.t for p in parts["v"]]
+    st.param = [p.t for p in prm]
+    for k in range(2):
+        st.m[k].zero_(); st.v[k].zero_(); st.master[k].fill_(0.01)
+    return st, prm + [p for v in parts.values() for p in v]
+
+
+@pytest.mark.parametrize("staging", [zr.STAGING_BULK, zr.STAGING_BULK_IO])
+def test_guards_bulk_staging(staging):
+    """Bulk-copy staging (loads, and loads + stores) writes nothing outside its buffers: ragged tensors, stages
+    of 256 elements so that tiles end in partial stages, the specialised (W = 2, 8) and generic (W = 3, A = 2)
+    kernels."""
+    numels = [12_345, 7, 40_000, 8, 999]
+    for W, A, dtype, shape in ((2, 1, zr.F16, (256, 2)), (8, 1, zr.BF16, (256, 3)), (3, 2, zr.BF16, (0, 0))):
+        plan = zr.Plan(numels, W=W, A=A, dtype=dtype, stage=2, cap=20_000, scaler=zr.Scaler(1.0))
+        plan.set_staging(staging, *shape)
+        assert plan.staging == staging
+        n = plan.numel
+        tdt = plan.torch_dtype()
+        grads = [Guarded(n, tdt) for _ in range(W * A)]
+        for g in grads:
+            g.t.normal_()
+        st, bufs = _guarded_state(n, tdt)
+        for _ in range(2):
+            plan.step([g.t for g in grads], st, HYPER)
+        torch.cuda.synchronize()
+        assert all(x.intact() for x in grads + bufs), (staging, W, A)
+        plan.close()
+
+
+def test_guards_in_place_step():
+    numels = [12_345, 7, 40_000, 8, 999]
+    for W, A in ((2, 1), (3, 2)):
+        plan = zr.Plan(numels, W=W, A=A, dtype=zr.F16, stage=1, cap=20_000, scaler=zr.Scaler(1.0))
+        n = plan.numel
+        grads = [Guarded(n, torch.float16) for _ in range(W * A)]
+        for g in grads:
+            g.t.normal_()
+        bufs = [Guarded(n, torch.float32) for _ in range(3)] + [Guarded(n, torch.float16)]
+        bufs[0].t.fill_(0.01); bufs[1].t.zero_(); bufs[2].t.zero_()
+        one = zr.State1.of(bufs[0].t, bufs[1].t, bufs[2].t, bufs[3].t)
+        plan.step_inplace([g.t for g in grads], one, HYPER)
+        torch.cuda.synchronize()
+        assert all(x.intact() for x in grads + bufs), (W, A)
+        plan.close()
+
+
 def test_guards_standalone_calls():
     rng_n = [1, 7, 9, 1000, 65_541]
     for n in rng_n:

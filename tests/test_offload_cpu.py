@@ -36,6 +36,32 @@ def test_offload_adamw_bit_exact(zr, dtype, nthreads):
         assert np.array_equal(out, oracle.encode(dtype, want[0]))
 
 
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("n", [1, 7, 8, 4095, 4097, 100_003])
+def test_offload_adamw_writes_nothing_outside(zr, dtype, n):
+    """Guard bands around every host array: the vectorised update, its cast passes (fp16 per 4096-element chunk)
+    and the thread split write only [0, n)."""
+    G = 64
+    rng = np.random.default_rng(n)
+
+    def guarded(dt, fill):
+        raw = np.empty(n + 2 * G, dt)
+        raw.view(np.uint8)[:] = 0xA5
+        raw[G:G + n] = fill
+        return raw
+
+    sums = guarded(F32, (rng.normal(size=n) * 10).astype(F32))
+    p, m = guarded(F32, 0.5), guarded(F32, 0.0)
+    v = guarded(F32, 0.0)
+    out = guarded(np.uint16, 0)
+    before = [a.copy() for a in (sums, p, m, v, out)]
+    assert zr.offload_adamw(sums[G:G + n], p[G:G + n], m[G:G + n], v[G:G + n], out[G:G + n], dtype, zr.AdamW(),
+                            1.0, 2, 1, 16) == 0
+    for a, b in zip((sums, p, m, v, out), before):
+        assert a[:G].tobytes() == b[:G].tobytes() and a[G + n:].tobytes() == b[G + n:].tobytes()
+    assert not np.array_equal(p[G:G + n], before[1][G:G + n])  # the update did run
+
+
 @pytest.mark.parametrize("bad", [np.nan, np.inf, -np.inf])
 @pytest.mark.parametrize("where", [0, 37_499, 37_500, 123_456, 299_999])
 def test_offload_adamw_skips_on_nonfinite(zr, bad, where):
