@@ -934,6 +934,10 @@ def main():
     if args.warmup < 3:
         print(f"bench: raising --warmup {args.warmup} to the minimum of 3", file=sys.stderr)
         args.warmup = 3
+    ws = _dist_env()[0]
+    if args.gpus != ws:
+        print(f"bench: --gpus {args.gpus} but {ws} process(es): N ranks come from torch.distributed.run "
+              f"(--nproc-per-node N); measuring with {ws}", file=sys.stderr)
     import zrgen
     w = zrgen.workload(args.workload)
     if args.second is None:
