@@ -501,6 +501,36 @@ def test_checkpoint_resume_is_byte_identical(staging):
             second.plan.restore(bad)
 
 
+@pytest.mark.parametrize("call", ["step", "step_inplace", "step_from_host"])
+def test_plan_without_parameters_steps_clean(call):
+    """Every tensor empty (the degenerate model): the reduce-scatter sums nothing, so each step is clean, as the
+    oracle's step over no buckets is: t and the good-step count advance and the scale grows on the interval
+    (the live set flips on the ping-pong paths). Zero-size tensors have null data pointers, which are accepted."""
+    numels = [0, 0, 0]
+    W = 2
+    plan = zr.Plan(numels, W=W, dtype=zr.F16, stage=1, cap=100,
+                   scaler=zr.Scaler(1024.0, dynamic=True, growth_interval=2))
+    ob, _ = oracle.bucket_plan(numels, 100, W)
+    assert plan.numel == 0 and len(plan.buckets) == 0 and ob.shape[0] == 0
+    osc = oracle.new_scaler(1024.0, dynamic=True, interval=2)
+    z, zu = np.zeros(0, np.float32), np.zeros(0, np.uint16)
+    grads = [torch.empty(0, dtype=torch.float16, device="cuda") for _ in range(W)]
+    st = plan.new_state1() if call == "step_inplace" else plan.new_state()
+    host = [torch.empty(0, dtype=torch.float16) for _ in range(W)]
+    for step in (1, 2, 3):
+        if call == "step":
+            rep = plan.step(grads, st, HYPER, report=True)
+        elif call == "step_inplace":
+            rep = plan.step_inplace(grads, st, HYPER, report=True)
+        else:
+            rep = plan.step_from_host(host, grads, st, HYPER)
+        orep, _ = oracle.step(W, 1, zr.F16, ob, [zu, zu], z, z.copy(), z.copy(), zu.copy(), OHYPER, osc)
+        assert rep.overflow == orep.overflow == 0
+        assert (rep.t, rep.good, rep.scale, rep.steps) == (osc.t, osc.good, osc.scale, step)
+        assert rep.current == (0 if call == "step_inplace" else step % 2)
+    plan.close()
+
+
 # ----------------------------------------------------------------------------- bulk-copy staging
 @pytest.mark.parametrize("W,A,dtype,shape", [(1, 1, zr.BF16, (0, 0)), (2, 1, zr.F16, (0, 0)),
                                              (2, 1, zr.BF16, (256, 2)), (3, 1, zr.F16, (0, 0)),

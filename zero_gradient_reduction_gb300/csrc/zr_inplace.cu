@@ -38,14 +38,17 @@ extern "C" zr_status zr_step_inplace(zr_plan* p, int stage, const void* const* g
   zr::clear_error();
   if (!p || !st || !h || !grads) return fail(ZR_ERR_INVALID, "zr_step_inplace: null argument");
   if (stage < 0 || stage > 3) return fail(ZR_ERR_INVALID, "zr_step_inplace: stage=%d not in 0..3", stage);
-  for (int r = 0; r < p->W * p->A; ++r)
-    if (!grads[r] || !zr::aligned16(grads[r]))
-      return fail(ZR_ERR_INVALID, "zr_step_inplace: grads[%d] null or misaligned", r);
-  if (!st->master || !st->m || !st->v || !st->param)
-    return fail(ZR_ERR_INVALID, "zr_step_inplace: the state set has a null array");
-  if (!zr::aligned16(st->master) || !zr::aligned16(st->m) || !zr::aligned16(st->v) || !zr::aligned16(st->param))
-    return fail(ZR_ERR_INVALID, "zr_step_inplace: the state set is misaligned");
-  if (p->ntiles == 0) return rep ? zr_plan_report(p, stream, rep) : ZR_OK;
+  // a plan with no parameters: empty (possibly null) arrays, and a step that only runs the
+  // scaler rule (two launches of one block over no tiles)
+  if (p->numel > 0) {
+    for (int r = 0; r < p->W * p->A; ++r)
+      if (!grads[r] || !zr::aligned16(grads[r]))
+        return fail(ZR_ERR_INVALID, "zr_step_inplace: grads[%d] null or misaligned", r);
+    if (!st->master || !st->m || !st->v || !st->param)
+      return fail(ZR_ERR_INVALID, "zr_step_inplace: the state set has a null array");
+    if (!zr::aligned16(st->master) || !zr::aligned16(st->m) || !zr::aligned16(st->v) || !zr::aligned16(st->param))
+      return fail(ZR_ERR_INVALID, "zr_step_inplace: the state set is misaligned");
+  }
 
   // The single set goes in both slots: the in-place kernel reads and writes slot 0 and
   // the flag pass touches neither.
@@ -75,7 +78,7 @@ extern "C" zr_status zr_step_inplace_from_host(zr_plan* p, int stage, const void
   if (!p || !host_grads || !dev_grads || !rep)
     return fail(ZR_ERR_INVALID, "zr_step_inplace_from_host: null argument");
   const int R = p->W * p->A;
-  for (int r = 0; r < R; ++r)
+  for (int r = 0; r < R && p->numel > 0; ++r)
     if (!host_grads[r] || !dev_grads[r] || !zr::aligned16(dev_grads[r]))
       return fail(ZR_ERR_INVALID, "zr_step_inplace_from_host: replica %d: null pointer or misaligned device buffer", r);
   if (!st || !h) return fail(ZR_ERR_INVALID, "zr_step_inplace_from_host: null argument");

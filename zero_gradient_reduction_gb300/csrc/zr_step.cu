@@ -413,6 +413,7 @@ static zr_status check_step_args(const zr_plan* p, int stage, const void* const*
                                  const zr_adamw_hyper* h) {
   if (!p || !st || !h || !grads) return fail(ZR_ERR_INVALID, "zr_step: null argument");
   if (stage < 0 || stage > 3) return fail(ZR_ERR_INVALID, "zr_step: stage=%d not in 0..3", stage);
+  if (p->numel == 0) return ZR_OK;  // no parameters: the arrays are empty and may be null
   for (int r = 0; r < p->W * p->A; ++r)
     if (!grads[r] || !zr::aligned16(grads[r])) return fail(ZR_ERR_INVALID, "zr_step: grads[%d] null or misaligned", r);
   for (int k = 0; k < 2; ++k) {
@@ -428,11 +429,13 @@ static zr_status check_step_args(const zr_plan* p, int stage, const void* const*
 }
 
 // One launch of the fused kernel over tiles [tile0, tile1) with `grid` blocks; the step's
-// launches add up to `total` blocks, and the last of those blocks decides the step.
+// launches add up to `total` blocks, and the last of those blocks decides the step. A plan
+// with no parameters has no tiles: its step is one block that only runs that decision
+// (a clean step), as the method's step over nothing is.
 static zr_status launch_step(zr_plan* p, int stage, const void* const* grads, const zr_state* st,
                              const zr_adamw_hyper* h, cudaStream_t s, int64_t tile0, int64_t tile1, int grid,
                              unsigned total) {
-  if (tile1 <= tile0 || grid < 1) return ZR_OK;
+  if (tile1 < tile0 || (tile1 == tile0 && p->ntiles > 0) || grid < 1) return ZR_OK;
   const FusedArgs a = make_args(p, stage, grads, st->master, st->m, st->v, st->param, h, tile0, tile1, total);
   reinterpret_cast<KernelFn>(p->kernel)<<<grid, kThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
@@ -488,13 +491,13 @@ extern "C" zr_status zr_step_from_host(zr_plan* p, int stage, const void* const*
   zr::clear_error();
   if (!p || !host_grads || !dev_grads || !rep) return fail(ZR_ERR_INVALID, "zr_step_from_host: null argument");
   const int R = p->W * p->A;
-  for (int r = 0; r < R; ++r)
+  for (int r = 0; r < R && p->numel > 0; ++r)
     if (!host_grads[r]) return fail(ZR_ERR_INVALID, "zr_step_from_host: host_grads[%d] is null", r);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   // Page-locked host memory the device can address (cudaHostAlloc, cudaHostRegister) is read
   // in place by the step kernel: each byte crosses the host link once and the HBM half of
   // the step overlaps the transfer. Anything else is copied into dev_grads first.
-  bool direct = true;
+  bool direct = p->numel > 0;
   const void* mapped[ZR_MAX_REPLICAS];
   for (int r = 0; r < R && direct; ++r) {
     cudaPointerAttributes at;
