@@ -249,8 +249,9 @@ zr_status zr_plan_reset(zr_plan* p, void* stream);
  * a, zr_plan_numel elements of the plan's dtype. rep: NULL for a fully asynchronous
  * call; otherwise the call synchronises `stream` and fills *rep. A plan whose tensors
  * are all empty (zr_plan_numel 0) reduces nothing: its step is clean (one block runs the
- * rule above), and its array pointers may be null; the same holds for zr_step_inplace
- * and the from-host variants.
+ * rule above), and its array pointers may be null; the same holds for zr_step_inplace,
+ * the from-host variants and zr_offload_step, and for zr_step_noalloc over buckets with
+ * no elements.
  * Errors: ZR_ERR_INVALID for a null plan/state/hyper, stage outside 0..3, null or
  * misaligned pointers, aliasing of the two state sets; ZR_ERR_CUDA. */
 zr_status zr_step(zr_plan* p, int stage, const void* const* grads, const zr_state* st,

@@ -124,3 +124,19 @@ def test_offload_random_plans_and_thread_counts(case):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (case, W, cap, nthreads)
     assert np.array_equal(u16(param_dev)[:n], o[3])
     plan.close()
+
+
+def test_offload_step_plan_without_parameters():
+    """Every tensor empty: nothing is reduced or copied, the step is clean, and the zero-size (null) arrays are
+    accepted, as zr_step accepts them."""
+    plan = zr.Plan([0, 0], W=2, dtype=zr.F16, stage=2, cap=100)
+    assert plan.numel == 0
+    e16 = torch.empty(0, dtype=torch.float16)
+    of = plan.offload_step([torch.empty(0, dtype=torch.float16, device="cuda")] * 2,
+                           torch.empty(0, device="cuda"), torch.empty(0), np.zeros(0, F32), np.zeros(0, F32),
+                           np.zeros(0, F32), e16, torch.empty(0, dtype=torch.float16, device="cuda"), zr.AdamW(),
+                           1.0, 1, nthreads=4)
+    torch.cuda.synchronize()
+    assert of == 0
+    plan.close()
+

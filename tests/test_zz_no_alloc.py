@@ -286,6 +286,12 @@ def test_noalloc_empty_and_warm_call_allocates_nothing(env):
     empty.call(t=1)
     torch.cuda.synchronize()
     assert int(empty.overflow.item()) == 0
+    # with nothing to reduce the arrays may be zero-size tensors, whose data pointers are null
+    of = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    zr.step_noalloc(np.zeros((0, 3), np.int64), 2, 1, zr.BF16, [torch.empty(0, dtype=torch.bfloat16, device="cuda")] * 2,
+                    zr.State(0, torch.bfloat16), 0, zr.AdamW(), 1.0, 1, of)
+    torch.cuda.synchronize()
+    assert int(of.item()) == 0
 
     run = Run(env, [100_000, 5_000], 4, 1, zr.BF16, 60_000, seed=10)
     run.step(1)  # first call on this device in a fresh process resolves the scratch address

@@ -194,23 +194,26 @@ extern "C" zr_status zr_step_noalloc(const zr_bucket* buckets, int nbuckets, int
     seen[w] = true;
     ord[p] = w;
   }
-  for (int r = 0; r < W * A; ++r)
-    if (!grads[r] || !zr::aligned16(grads[r]))
-      return fail(ZR_ERR_INVALID, "zr_step_noalloc: grads[%d] null or misaligned", r);
-  for (int k = 0; k < 2; ++k)
-    if (!st->master[k] || !st->m[k] || !st->v[k] || !st->param[k] || !zr::aligned16(st->master[k]) ||
-        !zr::aligned16(st->m[k]) || !zr::aligned16(st->v[k]) || !zr::aligned16(st->param[k]))
-      return fail(ZR_ERR_INVALID, "zr_step_noalloc: state set %d null or misaligned", k);
-  if (st->master[0] == st->master[1] || st->m[0] == st->m[1] || st->v[0] == st->v[1] || st->param[0] == st->param[1])
-    return fail(ZR_ERR_INVALID, "zr_step_noalloc: the two state sets must be distinct buffers");
   // every bucket must follow the ring rule
+  bool any = false;  // some bucket has elements (else the arrays are empty and may be null)
   for (int b = 0; b < nbuckets; ++b) {
+    any = any || buckets[b].len > 0;
     const zr_bucket& bk = buckets[b];
     if (bk.start < 0 || bk.len < 0 || (bk.start % ZR_ALIGN) || (bk.len % ZR_ALIGN) ||
         bk.chunk != zr_chunk_size(bk.len, W, ZR_ALIGN))
       return fail(ZR_ERR_INVALID, "zr_step_noalloc: bucket %d is not a ring bucket (start/len multiples of %d, "
                   "chunk = zr_chunk_size(len, W, %d))", b, ZR_ALIGN, ZR_ALIGN);
   }
+  for (int r = 0; r < W * A && any; ++r)
+    if (!grads[r] || !zr::aligned16(grads[r]))
+      return fail(ZR_ERR_INVALID, "zr_step_noalloc: grads[%d] null or misaligned", r);
+  for (int k = 0; k < 2 && any; ++k)
+    if (!st->master[k] || !st->m[k] || !st->v[k] || !st->param[k] || !zr::aligned16(st->master[k]) ||
+        !zr::aligned16(st->m[k]) || !zr::aligned16(st->v[k]) || !zr::aligned16(st->param[k]))
+      return fail(ZR_ERR_INVALID, "zr_step_noalloc: state set %d null or misaligned", k);
+  if (any && (st->master[0] == st->master[1] || st->m[0] == st->m[1] || st->v[0] == st->v[1] ||
+              st->param[0] == st->param[1]))
+    return fail(ZR_ERR_INVALID, "zr_step_noalloc: the two state sets must be distinct buffers");
   // the step kernel for (dtype, W, A) and the blocks of it that fit on the GPU at once
   KernelFn kern = dtype == ZR_F16 ? pick_kernel<zr::DT_F16, kPingPong>(W, A, false)
                                   : pick_kernel<zr::DT_BF16, kPingPong>(W, A, false);

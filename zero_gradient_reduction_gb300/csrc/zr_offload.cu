@@ -34,8 +34,10 @@ extern "C" zr_status zr_offload_step(zr_plan* p, int stage, const void* const* g
                                      void* stream, int32_t* overflow) {
   zr::Range range("zr_offload_step");
   zr::clear_error();
-  if (!p || !grads || !sums_dev || !sums_host || !master || !m || !v || !param_host || !param_dev || !h || !overflow)
-    return fail(ZR_ERR_INVALID, "zr_offload_step: null argument");
+  if (!p || !grads || !h || !overflow) return fail(ZR_ERR_INVALID, "zr_offload_step: null argument");
+  // a plan with no parameters has empty (possibly null) arrays
+  if (p->numel > 0 && (!sums_dev || !sums_host || !master || !m || !v || !param_host || !param_dev))
+    return fail(ZR_ERR_INVALID, "zr_offload_step: null array");
   if (stage < 0 || stage > 3) return fail(ZR_ERR_INVALID, "zr_offload_step: stage=%d not in 0..3", stage);
   if (p->A != 1) return fail(ZR_ERR_UNSUPPORTED, "zr_offload_step: plans with A > 1 (accumulate first)");
   if (t < 1) return fail(ZR_ERR_INVALID, "zr_offload_step: t must be >= 1");
