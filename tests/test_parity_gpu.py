@@ -252,9 +252,10 @@ class FusedRun:
     """A fused-step run on the GPU with the full oracle beside it (small sizes)."""
 
     def __init__(self, numels, W, A, dtype, cap, S, dynamic=False, order=None, seed=0, sigma=None, stage=2,
-                 interval=1000, staging=None):
+                 interval=1000, staging=None, backoff=0.5, growth=2.0, min_scale=1.0):
         self.plan = zr.Plan(numels, W=W, A=A, dtype=dtype, stage=stage, cap=cap, order=order,
-                            scaler=zr.Scaler(S, dynamic, growth_interval=interval))
+                            scaler=zr.Scaler(S, dynamic, backoff=backoff, growth=growth, min_scale=min_scale,
+                                             growth_interval=interval))
         if staging is not None:  # (staging, stage_elems, stages) for zr_plan_set_staging
             self.plan.set_staging(*staging)
         self.W, self.A, self.dtype, self.order = W, A, dtype, order
@@ -271,7 +272,8 @@ class FusedRun:
         self.grads = [torch.zeros(n, dtype=self.plan.torch_dtype(), device="cuda") for _ in range(W * A)]
         om = self.layout.master_host(0, n)
         self.o = [om, np.zeros(n, F32), np.zeros(n, F32), oracle.encode(dtype, om)]
-        self.osc = oracle.new_scaler(S, dynamic, interval=interval)
+        self.osc = oracle.new_scaler(S, dynamic, backoff=backoff, growth=growth, min_scale=min_scale,
+                                     interval=interval)
         self.S = S
         self.current = 0
 
@@ -374,6 +376,20 @@ def test_fused_scale_growth(staging):
         scales.append(rep.scale_used)
     assert scales == [4.0, 4.0, 8.0, 8.0, 16.0]
     run.check()
+
+
+@pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
+def test_scaler_floor_and_custom_rule(staging):
+    """A rule other than the default (backoff 0.25, growth 3, floor 2, interval 2): two skips in a row take the
+    scale 8 -> 2 -> 2 (floored, not 0.5), two clean steps then grow it to 6; state bit for bit the oracle's."""
+    run = FusedRun([4096, 1000], 2, 1, zr.F16, cap=10_000, S=8.0, dynamic=True, interval=2, backoff=0.25,
+                   growth=3.0, min_scale=2.0, seed=21, staging=None if staging is None else (staging, 0, 0))
+    want = [(8.0, 2.0, 1), (2.0, 2.0, 1), (2.0, 2.0, 0), (2.0, 6.0, 0), (6.0, 6.0, 0)]
+    for s, (used, nxt, skipped) in enumerate(want, start=1):
+        rep, _ = run.step(s, inject=(0, 17) if skipped else None)
+        assert (rep.scale_used, rep.scale, rep.overflow) == (used, nxt, skipped), s
+    assert rep.t == 3 and rep.skipped_total == 2
+    run.check("after the floor: ")
 
 
 @pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
