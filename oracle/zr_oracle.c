@@ -406,6 +406,9 @@ void zro_adamw(int64_t len, const float* g, float* p, float* m, float* v,
  * flag_override: -1 computes the flag from these buckets; 0/1 imposes a global
  * flag computed elsewhere (for runs over a sample of the buckets), OR-ed with
  * the local one. sums_out (nullable): the reduced fp32 sums, flat.
+ * With no buckets (a model without parameters) nothing is summed or flagged, so the
+ * step is clean: t, the beta products and the good-step count advance as for any
+ * clean step (the plain reading; the pages never meet this case).
  * Returns 0, or -1 on bad arguments, -2 on allocation failure, -3 if the
  * all-gathered replicas disagree. */
 int zro_step(int W, int A, int dtype, const int* order, int nbuckets, const zro_bucket* buckets,
