@@ -378,6 +378,19 @@ def test_fused_scale_growth(staging):
     run.check()
 
 
+@pytest.mark.parametrize("S,dtype", [(2.0 ** 126, zr.BF16), (2.0 ** -20, zr.F16)])
+@pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
+def test_extreme_loss_scales(S, dtype, staging):
+    """S = 2^126 at W = 3: r = fp32(1/(S*W)) is a subnormal fp32 factor (bf16 gradients near 1e36 still finite);
+    S = 2^-20 in fp16: the scaled gradients fall into fp16's subnormal range. Both bit for bit the oracle's."""
+    run = FusedRun([6000, 333, 9000], 3, 1, dtype, cap=10_000, S=S, seed=23,
+                   staging=None if staging is None else (staging, 0, 0))
+    for s in (1, 2):
+        rep, _ = run.step(s)
+        assert rep.overflow == 0
+    run.check(f"S = {S}: ")
+
+
 @pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
 def test_scaler_floor_and_custom_rule(staging):
     """A rule other than the default (backoff 0.25, growth 3, floor 2, interval 2): two skips in a row take the
