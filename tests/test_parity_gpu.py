@@ -252,7 +252,8 @@ class FusedRun:
     """A fused-step run on the GPU with the full oracle beside it (small sizes)."""
 
     def __init__(self, numels, W, A, dtype, cap, S, dynamic=False, order=None, seed=0, sigma=None, stage=2,
-                 interval=1000, staging=None, backoff=0.5, growth=2.0, min_scale=1.0):
+                 interval=1000, staging=None, backoff=0.5, growth=2.0, min_scale=1.0, hyper=None):
+        self.hyper, self.ohyper = hyper or (HYPER, OHYPER)
         self.plan = zr.Plan(numels, W=W, A=A, dtype=dtype, stage=stage, cap=cap, order=order,
                             scaler=zr.Scaler(S, dynamic, backoff=backoff, growth=growth, min_scale=min_scale,
                                              growth_interval=interval))
@@ -290,7 +291,7 @@ class FusedRun:
             self.grads[r].view(torch.int16)[i] = np.int16(np.uint16(bits).view(np.int16))
             ograds[r][i] = bits
         rep = self._launch(stage)
-        orep, _ = oracle.step(self.W, self.A, self.dtype, self.obuckets, ograds, *self.o, OHYPER, self.osc,
+        orep, _ = oracle.step(self.W, self.A, self.dtype, self.obuckets, ograds, *self.o, self.ohyper, self.osc,
                               order=self.order)
         assert rep.overflow == orep.overflow and rep.skipped == orep.skipped
         assert rep.scale_used == orep.scale_used and rep.scale == orep.scale_next
@@ -300,7 +301,7 @@ class FusedRun:
         return rep, orep
 
     def _launch(self, stage):
-        return self.plan.step(self.grads, self.state, HYPER, stage=stage, report=True)
+        return self.plan.step(self.grads, self.state, self.hyper, stage=stage, report=True)
 
     def live(self):
         L = self.state.live(self.current)
@@ -376,6 +377,53 @@ def test_fused_scale_growth(staging):
         scales.append(rep.scale_used)
     assert scales == [4.0, 4.0, 8.0, 8.0, 16.0]
     run.check()
+
+
+def _nan16(bits, dtype):
+    return (bits & 0x7FFF) > (0x7C00 if dtype == zr.F16 else 0x7F80)
+
+
+@pytest.mark.parametrize("dtype", [zr.F16, zr.BF16])
+@pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
+def test_non_finite_state_and_zero_over_zero(dtype, staging):
+    """Degenerate states: a caller's master holding NaN and +-inf, and eps = 0 with a zero gradient (0/0 in the
+    update). Results are NaN exactly where the oracle's are and bit-identical everywhere else. IEEE fixes neither
+    the sign nor the payload of a NaN made by arithmetic or by a conversion (x86, Arm and the GPU each make their
+    own), so NaN bits are the one thing not compared: the GPU's 16-bit cast writes one quiet NaN, the oracle's
+    encoder the quiet NaN of the value's sign."""
+    hyper = (zr.AdamW(lr=1e-3, beta1=0.9, beta2=0.999, eps=0.0, weight_decay=0.01),
+             oracle.AdamW(1e-3, 0.9, 0.999, 0.0, 0.01))
+    run = FusedRun([3000, 77, 5000], 2, 1, dtype, cap=6000, S=1.0, seed=29, hyper=hyper,
+                   staging=None if staging is None else (staging, 0, 0))
+    planted = {11: np.nan, 12: -np.nan, 13: np.inf, 14: -np.inf, 4000: np.nan}
+    for i, x in planted.items():
+        run.state.master[0][i] = float(x)
+        run.o[0][i] = np.float32(x)
+    zero_at = [100, 101, 5003]
+    for s in (1, 2):
+        st = torch.cuda.current_stream().cuda_stream
+        for r in range(2):
+            run.layout.grads_dev(run.grads[r], s, r, run.S, run.table, st)
+        ograds = [run.layout.grads_host(0, run.n, s, r, run.S) for r in range(2)]
+        for r in range(2):
+            for i in zero_at:  # every worker's gradient exactly zero here: 0/0 once m and v are zero
+                run.grads[r][i] = 0.0
+                ograds[r][i] = 0
+        rep = run._launch(None)
+        orep, _ = oracle.step(2, 1, dtype, run.obuckets, ograds, *run.o, run.ohyper, run.osc)
+        assert rep.overflow == orep.overflow == 0 and rep.t == orep.t_after
+        run.current = rep.current
+    gm, gmm, gv, gp = run.live()
+    om, omm, ov, op = run.o
+    for name, g, o in (("master", gm, om), ("m", gmm, omm), ("v", gv, ov)):
+        gn, on = np.isnan(g), np.isnan(o)
+        assert np.array_equal(gn, on), name
+        assert np.array_equal(g[~gn].view(np.uint32), o[~on].view(np.uint32)), name
+    # NaN at least where planted and where the gradient is zero (alignment padding, also zero, joins them)
+    assert {11, 12, 4000, *zero_at} <= set(np.flatnonzero(np.isnan(gm)).tolist())
+    assert np.isposinf(gm[13]) and np.isneginf(gm[14])
+    gnan, onan = _nan16(gp, dtype), _nan16(op, dtype)
+    assert np.array_equal(gnan, onan) and np.array_equal(gp[~gnan], op[~onan])
 
 
 @pytest.mark.parametrize("S,dtype", [(2.0 ** 126, zr.BF16), (2.0 ** -20, zr.F16)])
