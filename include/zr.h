@@ -95,7 +95,10 @@ int64_t zr_chunk_size(int64_t n, int W, int align);
  * never split; a non-empty bucket closes before a tensor that would take it past
  * cap_elems, so a tensor larger than the cap sits alone. Buckets are contiguous.
  * out: caller array of at least ntensors entries (host); *nbuckets: count written;
- * tensor_offsets[ntensors]: flat offset of each tensor (host, may be NULL).
+ * tensor_offsets[ntensors]: flat offset of each tensor (host, may be NULL). The gaps
+ * that align tensors are elements of the flat arrays like any other: the ring sums,
+ * the overflow flag and the update cover them, so a caller keeps them finite in its
+ * gradient buffers (zero, as a zero-initialised buffer leaves them).
  * Errors: ZR_ERR_INVALID for null out/nbuckets, ntensors < 0, a negative numel,
  * cap_elems < 1, W outside [1, ZR_MAX_W], align < 1. */
 zr_status zr_bucket_plan(const int64_t* numels, int ntensors, int64_t cap_elems, int W, int align,

@@ -368,6 +368,24 @@ def test_fused_skip_then_resume(staging):
 
 
 @pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
+def test_non_finite_in_an_alignment_gap_skips(staging):
+    """The gaps that align tensors to 8 elements are elements of the flat buffers: a +inf left in one is summed
+    and flagged like any other, on both sides, and the step is skipped."""
+    numels = [1, 7, 3000]
+    run = FusedRun(numels, 2, 1, zr.BF16, cap=10_000, S=1.0, seed=31,
+                   staging=None if staging is None else (staging, 0, 0))
+    gaps = [i for i in range(run.n) if not any(o <= i < o + k for o, k in zip(run.ooffsets, numels))]
+    assert gaps
+    run.step(1)
+    rep, orep = run.step(2, inject=(1, gaps[0]))
+    assert rep.overflow == orep.overflow == 1
+    run.grads[1].view(torch.int16)[gaps[0]] = 0  # the caller clears it again
+    rep, _ = run.step(3)
+    assert rep.overflow == 0
+    run.check()
+
+
+@pytest.mark.parametrize("staging", [None, zr.STAGING_BULK])
 def test_fused_scale_growth(staging):
     run = FusedRun([4096, 1000], 2, 1, zr.BF16, cap=10_000, S=4.0, dynamic=True, interval=2,
                    staging=None if staging is None else (staging, 0, 0))
