@@ -912,20 +912,24 @@ def run_zr(args, w):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", choices=["zr", "reference"], default="zr")
-    ap.add_argument("--workload", default=WORKLOAD_DEFAULT)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs of the job: one rank each, launched by torch.distributed.run (independent replicas)")
+    ap.add_argument("--steps", type=int, default=100, help="timed steps")
+    ap.add_argument("--warmup", type=int, default=5, help="untimed steps before them (at least 3)")
+    ap.add_argument("--impl", choices=["zr", "reference"], default="zr",
+                    help="zr: this library on the GPU; reference: the oracle on the host cores")
+    ap.add_argument("--workload", default=WORKLOAD_DEFAULT,
+                    help="7b, 1p3b, gpt2, gpt2_W<W>, tiny, 13b, 7b_slice or sweep_W{2,4,8}_cap2^{19..28}")
     ap.add_argument("--second", default=None,
                     help=f"a second workload timed after the first, on freed memory (default: {SECOND_DEFAULT} when "
                          f"the workload is {WORKLOAD_DEFAULT}; 'none' for no second workload)")
-    ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-chain", action="store_true")
-    ap.add_argument("--chain-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=3, help="steps of the end-to-end leg (host gradients)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target seconds of the oracle's CPU baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="leave out the end-to-end leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="leave out the oracle's CPU baseline")
+    ap.add_argument("--no-chain", action="store_true",
+                    help="leave out the side measurements (unfused chain, ZeRO-3 gather, in place, overlap, offload)")
+    ap.add_argument("--chain-steps", type=int, default=5, help="steps of the unfused chain")
     ap.add_argument("--staging", choices=["bulk", "bulk_io", "registers"], default=None,
                     help="load staging of the main step's zr_step (default: the plan's own choice)")
     ap.add_argument("--inplace", action="store_true",
