@@ -16,6 +16,7 @@ zr_step_from_host with pinned host gradients (e2e).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -828,7 +829,7 @@ def run_zr(args, w):
             r = e2e_step()
         dt = max_over_ranks(time.perf_counter() - t0, ws, dev)
         e2e = {"value": whole_job_rate(plan.n_real * args.e2e_steps, dt, ws), "unit": "Gparams/s",
-               "h2d_bytes_per_step": int(2 * n * w.W * w.A), "d2h_bytes_per_step": int(__import__("ctypes").sizeof(r)),
+               "h2d_bytes_per_step": int(2 * n * w.W * w.A), "d2h_bytes_per_step": int(ctypes.sizeof(r)),
                "ms_per_step": dt / args.e2e_steps * 1e3, "steps": args.e2e_steps, "api": api}
         # the host link itself: one large pinned copy per direction (cudaMemcpyAsync through torch), CUDA events
         link = _link_rates(torch, host[0], grads[0], dev, stream)
