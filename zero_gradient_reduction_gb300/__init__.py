@@ -126,6 +126,8 @@ def lib():
                 "zr_step_from_host": (st, [vp, i32, vp, vp, ctypes.POINTER(StateC), ctypes.POINTER(Hyper), vp,
                                            ctypes.POINTER(StepReport)]),
                 "zr_plan_report": (st, [vp, vp, ctypes.POINTER(StepReport)]),
+                "zr_step_noalloc": (st, [vp, i32, i32, i32, i32, vp, vp, ctypes.POINTER(StateC), i32,
+                                         ctypes.POINTER(Hyper), ctypes.c_float, i64, vp, vp]),
                 "zr_plan_checkpoint": (st, [vp, vp, ctypes.POINTER(Checkpoint)]),
                 "zr_plan_restore": (st, [vp, ctypes.POINTER(Checkpoint), vp]),
                 "zr_model_state_bytes": (i64, [i32, i64, i32]),
@@ -561,10 +563,6 @@ def step_noalloc(buckets: np.ndarray, W: int, A: int, dtype: int, grads: Sequenc
     """zr_step_noalloc: the fused step for callers that cannot allocate device memory (scratch lives in a
     static device array of the library; the caller carries the live set, the scale and t)."""
     fn = lib().zr_step_noalloc
-    fn.restype = ctypes.c_int
-    fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
-                   ctypes.c_void_p, ctypes.POINTER(StateC), ctypes.c_int, ctypes.POINTER(Hyper), ctypes.c_float,
-                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
     b = np.asarray(buckets, dtype=np.int64).reshape(-1, 3)
     table = (Bucket * max(len(b), 1))(*[Bucket(int(s), int(n), int(c)) for s, n, c in b])
     ordc = (ctypes.c_int * W)(*order) if order is not None else None
