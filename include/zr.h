@@ -302,20 +302,26 @@ zr_status zr_plan_set_bucket_blocks(zr_plan* p, int max_blocks);
  * one-dimensional bulk copies (cp.async.bulk, this GPU's memory only) completed on mbarriers,
  * keeping `stages` stages in flight, and eight consumer warps compute from shared memory.
  * Both give the same bytes; only speed differs. Bulk staging covers zr_step (and its CUDA
- * graph capture) for plans with 16-bit gradients (any W and A: a stage holds the W*A
- * replica slices), and is what zr_plan_create chooses when the automatic shape keeps
- * stages of 2048 elements (W*A <= 8) and the plan has at least four waves of tiles (a plan
- * that streams from HBM); other plans, and the other calls, use register staging.
+ * graph capture) for plans with 16-bit gradients and any W and A: with W*A <= 8 a stage
+ * holds all W*A replica slices of its elements; with more, the slices of a range of
+ * elements follow one another in stages of 8 slices (at most 2048 elements each), the
+ * consumers carrying their running sums from one stage to the next in the same order.
+ * It is what zr_plan_create chooses when the automatic shape keeps stages of 2048
+ * elements with all slices in one stage (W*A <= 8) and the plan has at least four waves
+ * of tiles (a plan that streams from HBM); other plans, and the other calls, use register
+ * staging (with W*A > 8 it measured as fast or faster).
  * stage_elems = 0 and stages = 0 choose a shape that lets two blocks share an SM. Call it
  * between steps; a CUDA graph captured earlier keeps the kernel it captured.
  * Every wait of a bulk-staged step is bounded (2 s); one that gives up skips the step and
  * makes zr_plan_report (and zr_step with a report) return ZR_ERR_TIMEOUT until
  * zr_plan_reset. Errors: ZR_ERR_INVALID (null plan, unknown staging, stage_elems not 0 or a
- * multiple of 8 up to 65536, stages above 4), ZR_ERR_UNSUPPORTED (fp32 gradients, a shape
- * that does not fit an SM's shared memory), ZR_ERR_CUDA.
- * ZR_STAGING_BULK_IO: as ZR_STAGING_BULK, and the results go out the same way: the consumers
- * write each stage's new master/m/v and 16-bit parameter back into its shared-memory slots
- * and a storer warp copies them to state set 1-k with bulk copies (shared to global). */
+ * multiple of 8 up to 65536, or up to 2048 for ZR_STAGING_BULK with W*A > 8, stages above
+ * 4), ZR_ERR_UNSUPPORTED (fp32 gradients, a shape that does not fit an SM's shared memory),
+ * ZR_ERR_CUDA.
+ * ZR_STAGING_BULK_IO: as ZR_STAGING_BULK (every slice of its elements in one stage, for any
+ * W*A), and the results go out the same way: the consumers write each stage's new
+ * master/m/v and 16-bit parameter back into its shared-memory slots and a storer warp
+ * copies them to state set 1-k with bulk copies (shared to global). */
 typedef enum { ZR_STAGING_REGISTERS = 0, ZR_STAGING_BULK = 1, ZR_STAGING_BULK_IO = 2 } zr_staging;
 zr_status zr_plan_set_staging(zr_plan* p, int staging, int stage_elems, int stages);
 /* The staging zr_step uses for plan p (a zr_staging value); -1 for a null plan. */

@@ -51,9 +51,13 @@ def test_random_plan_matches_oracle(case):
     if pick >= 2 and rng.integers(0, 2):
         E = int(rng.choice([256, 512, 1024, 2048, 4096]))
         NS = int(rng.integers(1, 5))
-        while NS > 1 and NS * (2 * W * A * E + 12 * E) > 200 * 1024:
+        # bulk loads with more than 8 replica slices spread them over stages of 8 (stages of at most 2048)
+        chunked = pick == 2 and W * A > 8
+        E = min(E, 2048) if chunked else E
+        stage_bytes = (lambda e: 2 * 8 * e + 12 * e) if chunked else (lambda e: 2 * W * A * e + 12 * e)
+        while NS > 1 and NS * stage_bytes(E) > 200 * 1024:
             NS -= 1
-        while E > 256 and NS * (2 * W * A * E + 12 * E) > 200 * 1024:
+        while E > 256 and NS * stage_bytes(E) > 200 * 1024:
             E //= 2
         staging = (staging[0], E, NS)
     run = cls(numels, W, A, dtype, cap=cap, S=S, dynamic=dynamic, order=order, seed=case, sigma=sigma,

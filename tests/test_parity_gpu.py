@@ -729,6 +729,12 @@ def test_bulk_staging_rejects_unsupported():
     with pytest.raises(zr.ZrError):  # 4 stages of 65536 elements do not fit an SM
         plan.set_staging(zr.STAGING_BULK, 65536, 4)
     plan.close()
+    plan = zr.Plan([4096], W=16, A=1, dtype=zr.BF16, stage=2, cap=8192)
+    with pytest.raises(zr.ZrError):  # more than 8 replica slices: stages of 8 slices, at most 2048 elements
+        plan.set_staging(zr.STAGING_BULK, 4096, 1)
+    plan.set_staging(zr.STAGING_BULK, 2048, 1)
+    plan.set_staging(zr.STAGING_BULK_IO, 4096, 1)  # the load + store variant keeps one stage for all slices
+    plan.close()
     # a refused call leaves no CUDA error behind for the caller's next check
     x = torch.empty(1024, device="cuda")
     x.fill_(1.0)

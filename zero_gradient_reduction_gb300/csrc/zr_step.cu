@@ -30,6 +30,7 @@ void take_cuda_error() { (void)cudaGetLastError(); }
 #include "zr_plan.h"
 #include "zr_step_kernel.cuh"
 #include "zr_step_bulk.cuh"
+#include "zr_step_bulk_chunked.cuh"
 
 namespace {
 
@@ -96,6 +97,17 @@ void zr::bulk_auto_shape(int R, int* E, int* NS) {
 // fill costs more than it hides (the 786,432-param workload: 14.5 us against 12.5 us).
 bool zr::bulk_preferred(int E, int64_t ntiles, int64_t resident) { return E >= 2048 && ntiles >= 4 * resident; }
 
+// Automatic shape of the chunked stages (more than kChunkSlices replica slices per element):
+// 2048 elements, as many stages as kBulkBudget holds (two of 56 KB), up to kBulkMaxStages.
+static void chunked_auto_shape(int* E, int* NS) {
+  constexpr int kBulkBudget = 113 * 1024;
+  if (*E == 0) *E = kChunkMaxElems;
+  if (*NS == 0) {
+    const int ns = kBulkBudget / chunked_stage_bytes(*E);
+    *NS = ns < 1 ? 1 : ns > kBulkMaxStages ? kBulkMaxStages : ns;
+  }
+}
+
 // Chooses how zr_step stages its loads (the body of zr_plan_set_staging; zr_plan_create
 // also calls it to make bulk staging the default where it applies).
 static zr_status configure_staging(zr_plan* p, int staging, int stage_elems, int stages) {
@@ -107,14 +119,19 @@ static zr_status configure_staging(zr_plan* p, int staging, int stage_elems, int
     return fail(ZR_ERR_INVALID, "zr_plan_set_staging: unknown staging %d", staging);
   const bool sb = staging == ZR_STAGING_BULK_IO;
   if (p->fp32_grads) return fail(ZR_ERR_UNSUPPORTED, "zr_plan_set_staging: bulk staging needs 16-bit gradients");
-  const int R = p->W * p->A;  // replica slices per stage
-  if (stage_elems < 0 || (stage_elems % 8) != 0 || stage_elems > 65536)
-    return fail(ZR_ERR_INVALID, "zr_plan_set_staging: stage_elems must be 0 or a multiple of 8 up to 65536");
+  const int R = p->W * p->A;  // replica slices per element
+  // more slices than one stage takes: the chunked kernel spreads them over consecutive stages
+  const bool chunked = !sb && R > kChunkSlices;
+  const int max_elems = chunked ? kChunkMaxElems : 65536;
+  if (stage_elems < 0 || (stage_elems % 8) != 0 || stage_elems > max_elems)
+    return fail(ZR_ERR_INVALID, "zr_plan_set_staging: stage_elems must be 0 or a multiple of 8 up to %d%s", max_elems,
+                chunked ? " (stages of 8 replica slices)" : "");
   if (stages < 0 || stages > kBulkMaxStages)
     return fail(ZR_ERR_INVALID, "zr_plan_set_staging: stages must be 0 or 1..%d", kBulkMaxStages);
   int E = stage_elems, NS = stages;
-  zr::bulk_auto_shape(R, &E, &NS);
-  const int64_t smem64 = (int64_t)NS * bulk_stage_bytes(R, E);
+  if (chunked) chunked_auto_shape(&E, &NS);
+  else zr::bulk_auto_shape(R, &E, &NS);
+  const int64_t smem64 = (int64_t)NS * (chunked ? chunked_stage_bytes(E) : bulk_stage_bytes(R, E));
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
   if (e != cudaSuccess) return cuda_fail("zr_plan_set_staging", e);
@@ -124,6 +141,8 @@ static zr_status configure_staging(zr_plan* p, int staging, int stage_elems, int
   const int smem = (int)smem64;
   BulkKernelFn k = sb ? (p->dtype == ZR_F16 ? pick_bulk_kernel<zr::DT_F16, true>(p->W, p->A)
                                             : pick_bulk_kernel<zr::DT_BF16, true>(p->W, p->A))
+                 : chunked ? (p->dtype == ZR_F16 ? pick_chunked_kernel<zr::DT_F16>(p->A)
+                                                 : pick_chunked_kernel<zr::DT_BF16>(p->A))
                       : (p->dtype == ZR_F16 ? pick_bulk_kernel<zr::DT_F16, false>(p->W, p->A)
                                             : pick_bulk_kernel<zr::DT_BF16, false>(p->W, p->A));
   const int threads = bulk_threads(sb);
@@ -297,7 +316,7 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
   // zr_step stages its loads by bulk copies where zr::bulk_preferred says so; other plans
   // keep register staging.
   if (!p->fp32_grads && p->ntiles > 0) {
-    if (configure_staging(p, ZR_STAGING_BULK, 0, 0) != ZR_OK ||
+    if (p->W * p->A > kChunkSlices || configure_staging(p, ZR_STAGING_BULK, 0, 0) != ZR_OK ||
         !zr::bulk_preferred(p->bulk_E, p->ntiles, p->bulk_resident))
       p->staging = ZR_STAGING_REGISTERS;
     zr::clear_error();
