@@ -23,8 +23,9 @@ CU = ["zr_step.cu", "zr_inplace.cu", "zr_collectives.cu", "zr_noalloc.cu", "zr_z
 CPP = ["zr_host.cpp", "zr_offload_host.cpp"]
 # the host AdamW of ZeRO-Offload: vectorised (no errno on sqrt), still one rounding per op
 CPP_EXTRA = {"zr_offload_host.cpp": ["-O3", "-fno-math-errno", "-pthread"]}
-HEADERS = [os.path.join(INCLUDE, "zr.h"), os.path.join(CSRC, "zr_internal.h"), os.path.join(CSRC, "zr_device.cuh"),
-           os.path.join(CSRC, "zr_step_kernel.cuh"), os.path.join(CSRC, "zr_plan.h"), os.path.join(CSRC, "zr_nvtx.h")]
+# every header a translation unit may include: a change to any of them rebuilds all units
+HEADERS = [os.path.join(INCLUDE, "zr.h")] + sorted(
+    os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh")))
 
 
 def _nvcc_flags(verbose_ptxas: bool = False):
