@@ -314,7 +314,8 @@ extern "C" zr_status zr_plan_create(const zr_plan_desc* d, zr_plan** out) {
     return ss;
   }
   // zr_step stages its loads by bulk copies where zr::bulk_preferred says so; other plans
-  // keep register staging.
+  // keep register staging, and so do plans with more than kChunkSlices replica slices per
+  // element, whose chunked bulk stages measured as fast as register staging at best.
   if (!p->fp32_grads && p->ntiles > 0) {
     if (p->W * p->A > kChunkSlices || configure_staging(p, ZR_STAGING_BULK, 0, 0) != ZR_OK ||
         !zr::bulk_preferred(p->bulk_E, p->ntiles, p->bulk_resident))
