@@ -684,20 +684,21 @@ def test_bulk_staging_large_plan_one_block_per_tile(mode):
         run.check(f"large bulk step {s}: ")
 
 
-@pytest.mark.parametrize("mode", [zr.STAGING_BULK, zr.STAGING_BULK_IO])
-def test_bulk_wait_timeout_reports_and_recovers(mode):
+@pytest.mark.parametrize("mode,W", [(zr.STAGING_BULK, 2), (zr.STAGING_BULK_IO, 2), (zr.STAGING_BULK, 16)])
+def test_bulk_wait_timeout_reports_and_recovers(mode, W):
     """The bounded waits of bulk staging: with the test hook on, no stage's copies complete its barrier, so every
     wait runs out after its limit (2 s), the step is skipped with the live set unchanged, zr_plan_report returns
     ZR_ERR_TIMEOUT and the CUDA context stays usable; restoring the step state clears the error and the run
     continues, bit-exact against the oracle."""
     import time
-    run = FusedRun([40_000, 3_000], 2, 1, zr.F16, cap=50_000, S=1024.0, seed=31, staging=(mode, 0, 0))
+    # W = 16 under ZR_STAGING_BULK runs the chunked kernel (stages of 8 replica slices)
+    run = FusedRun([40_000, 3_000], W, 1, zr.F16, cap=50_000, S=1024.0, seed=31, staging=(mode, 0, 0))
     run.step(1)
     run.check("before the stalled step: ")
     ck = run.plan.checkpoint()
     before = [x.copy() for x in run.live()]
     cs = torch.cuda.current_stream().cuda_stream
-    for r in range(2):
+    for r in range(W):
         run.layout.grads_dev(run.grads[r], 2, r, run.S, run.table, cs)
     assert zr.lib().zr_plan_stall_bulk_waits(run.plan._h, 1) == 0
     t0 = time.perf_counter()
